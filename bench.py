@@ -1,0 +1,408 @@
+"""Benchmark of the quantized paged KV cache hot path.
+
+One step = one decode layer per cache format of the Llama-3-8B-shaped
+workload (32 sequences x 4096 context, 32 query / 8 KV heads, head_dim 128,
+block_size 16; formats bf16, fp8 with a per-tensor scale, turbo4): for each
+format, the cache write of that step's 32 new tokens (one per sequence, at
+position 4095) followed by the split-K paged decode over all 4096 positions.
+The caches (956 MB in total, far above the 129 MB L2) are filled before the
+timed region with the same write kernel.
+
+value  = algorithmic bytes of the step / step time, in GB/s.  Algorithmic
+         bytes = cache bytes the decode must read (every attended K/V row of
+         every KV head, data + scales) + the write's input rows read and
+         cache rows written.
+e2e    = the same bytes / step time measured through the public API with the
+         step's inputs copied from pinned host memory and the outputs copied
+         back inside the timed region.
+roofline: the dominant kernel (the split-K decode of the bf16 layer, the
+         largest share of the step) against the measured HBM copy bandwidth.
+cpu_baseline: the CPU oracle (numpy) decoding a bounded sample of the same
+         workload.
+
+``--impl reference`` times the CPU oracle alone on that workload and prints
+its line (the pages ship no runnable implementation).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode HBM GB/s (cache bytes read / time), us/layer, cache-write GB/s"
+WORKLOAD = "llama8b"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic_decode_bytes(fmt, seq_lens, nkv, hd, bs, window=0):
+    from quantized_paged_kv_reshape_gb300 import ops
+    per_tok = 0
+    for side in (0, 1):
+        per_tok += ops.block_bytes(fmt, side, bs, nkv, hd) // bs   # bytes per token (all heads)
+    lens = np.asarray(seq_lens, np.int64)
+    att = np.minimum(lens, window) if window > 0 else lens
+    return int(att.sum()) * per_tok
+
+
+def write_bytes(fmt, ntok, nkv, hd, bs, in_bytes=2):
+    from quantized_paged_kv_reshape_gb300 import ops
+    out = sum(ops.block_bytes(fmt, side, bs, nkv, hd) // bs for side in (0, 1)) * ntok
+    return 2 * ntok * nkv * hd * in_bytes + out + 8 * ntok
+
+
+# --------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    from quantized_paged_kv_reshape_gb300 import ops, workloads as W
+    from quantized_paged_kv_reshape_gb300 import _abi
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    _abi.lib()
+
+    w = W.make(WORKLOAD, seed=rank)
+    nkv, nq, hd, bs = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size
+    nseq = w.num_seqs
+    L = int(w.seq_lens[0])
+    tables_np = W.block_tables(w)
+    mb = tables_np.shape[1]
+    tables = torch.from_numpy(tables_np).to(dev)
+    lens = torch.from_numpy(w.seq_lens).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + rank)
+
+    # K/V of every cached position: bf16 N(0,1) * per-channel scale (lognormal
+    # sigma 0.5, 1% of channels x10), drawn on the device.
+    ch_k = torch.from_numpy(W.channel_scales(w, 0)).to(dev)
+    ch_v = torch.from_numpy(W.channel_scales(w, 1)).to(dev)
+    ntok = nseq * L
+    slots_all = torch.from_numpy(W.slot_mapping_for_sequences(w, tables_np)).to(dev)
+    kall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_k).to(torch.bfloat16)
+    vall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_v).to(torch.bfloat16)
+    k_scale = float(kall.float().abs().amax()) / 448.0
+    v_scale = float(vall.float().abs().amax()) / 448.0
+
+    fmts = list(w.formats)
+    pools = {}
+    write_ms = {}
+    for f in fmts:
+        kp = ops.alloc_pool(w.num_blocks, f, 0, bs, nkv, hd, device=dev)
+        vp = ops.alloc_pool(w.num_blocks, f, 1, bs, nkv, hd, device=dev)
+        pools[f] = (kp, vp)
+        kf, vf = kall.view(ntok, -1), vall.view(ntok, -1)
+        for rep in range(3):  # fill (the last two timed: full-cache write throughput)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ops.cache_write(kf, vf, kp, vp, slots_all, f, nkv, hd, bs, k_scale=k_scale,
+                            v_scale=v_scale)
+            e1.record()
+            torch.cuda.synchronize()
+            if rep:
+                write_ms.setdefault(f, []).append(e0.elapsed_time(e1))
+
+    # Step inputs: the new token of every sequence (position L-1) and its query.
+    q = (torch.randn((nseq, nq, hd), generator=g, device=dev)).to(torch.bfloat16)
+    knew = kall.view(nseq, L, nkv, hd)[:, L - 1].contiguous()
+    vnew = vall.view(nseq, L, nkv, hd)[:, L - 1].contiguous()
+    slots_new = slots_all.view(nseq, L)[:, L - 1].contiguous()
+    outs = {f: torch.empty((nseq, nq, hd), dtype=torch.float32, device=dev) for f in fmts}
+    wsp = {f: ops.alloc_workspace(nseq, nq, nkv, hd, bs, mb, 0, f, device=dev) for f in fmts}
+    del kall, vall
+
+    stream = torch.cuda.current_stream()
+    ev = {f: [] for f in fmts}
+
+    def step(record=False):
+        for f in fmts:
+            kp, vp = pools[f]
+            ops.cache_write(knew.view(nseq, -1), vnew.view(nseq, -1), kp, vp, slots_new, f, nkv,
+                            hd, bs, k_scale=k_scale, v_scale=v_scale)
+            if record:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            ops.paged_decode(q, kp, vp, tables, lens, f, nkv, bs, out=outs[f], k_scale=k_scale,
+                             v_scale=v_scale, workspace=wsp[f])
+            if record:
+                b.record(stream)
+                ev[f].append((a, b))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_total = t0.elapsed_time(t1)
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+
+    # e2e through the public API: pinned host inputs -> device, outputs -> host.
+    h_q = q.cpu().pin_memory()
+    h_k = knew.cpu().pin_memory()
+    h_v = vnew.cpu().pin_memory()
+    h_slots = slots_new.cpu().pin_memory()
+    h_tab = tables.cpu().pin_memory()
+    h_lens = lens.cpu().pin_memory()
+    h_out = {f: torch.empty((nseq, nq, hd), dtype=torch.float32).pin_memory() for f in fmts}
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(knew), torch.empty_like(vnew)
+    d_slots, d_tab, d_lens = torch.empty_like(slots_new), torch.empty_like(tables), torch.empty_like(lens)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tab, h_lens))
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        for src, dst in ((h_q, d_q), (h_k, d_k), (h_v, d_v), (h_slots, d_slots), (h_tab, d_tab),
+                         (h_lens, d_lens)):
+            dst.copy_(src, non_blocking=True)
+        for f in fmts:
+            kp, vp = pools[f]
+            ops.cache_write(d_k.view(nseq, -1), d_v.view(nseq, -1), kp, vp, d_slots, f, nkv, hd,
+                            bs, k_scale=k_scale, v_scale=v_scale)
+            ops.paged_decode(d_q, kp, vp, d_tab, d_lens, f, nkv, bs, out=outs[f],
+                             k_scale=k_scale, v_scale=v_scale, workspace=wsp[f])
+            h_out[f].copy_(outs[f], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(10, args.steps // 4)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e_steps
+
+    ms_step = ms_total / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_step, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+
+    dec_bytes = {f: algorithmic_decode_bytes(f, w.seq_lens, nkv, hd, bs) for f in fmts}
+    step_bytes = sum(dec_bytes.values()) + sum(write_bytes(f, nseq, nkv, hd, bs) for f in fmts)
+    peak, peak_kind = peaks()
+    per_fmt = {}
+    for f in fmts:
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev[f]) * 1e3
+        gbs = dec_bytes[f] / (us * 1e-6) / 1e9
+        wms = statistics.mean(write_ms[f])
+        per_fmt[f] = {"us_per_layer": round(us, 2), "decode_gbs": round(gbs, 1),
+                      "frac_of_peak": round(gbs / peak, 4),
+                      "cache_bytes": dec_bytes[f],
+                      "write_gbs": round(write_bytes(f, ntok, nkv, hd, bs) / (wms * 1e-3) / 1e9, 1),
+                      "write_us_131072_tokens": round(wms * 1e3, 1)}
+    dom = max(fmts, key=lambda f: per_fmt[f]["us_per_layer"])
+    value = step_bytes * ws / (ms_step * 1e-3) / 1e9
+    e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
+    launches_per_step = 3 * len(fmts)   # write + decode split + combine per format
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "llama8b decode layer: 32 seqs x 4096 ctx, 32 q / 8 kv heads, "
+                               "head_dim 128, block_size 16; one layer per format bf16, fp8, turbo4",
+                   "formats": fmts, "l2": "inputs larger than L2 (956 MB of cache per step)",
+                   "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
+        "per_format": per_fmt,
+        "roofline": {"kernel": f"decode_split_kernel ({dom})", "bound": "hbm",
+                     "achieved": per_fmt[dom]["decode_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": round(per_fmt[dom]["decode_gbs"] / peak, 4),
+                     "traffic": None, "peak_kind": peak_kind + " (hbm_gbs copy)",
+                     "timed": "split + combine kernels per launch, CUDA events on the launch stream"},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        print(json.dumps(line))
+
+
+# --------------------------------------------------------------------- CPU oracle
+
+class OracleSample:
+    """One sequence of the workload (``ntok`` positions x 8 kv / 32 q heads,
+    turbo4) written and decoded by the CPU oracle."""
+
+    def __init__(self, ntok=4096, fmt="turbo4"):
+        import oracle
+        from quantized_paged_kv_reshape_gb300 import workloads as W
+        self.oracle, self.fmt = oracle, fmt
+        w = W.make(WORKLOAD, num_seqs=1, seq_lens=np.array([ntok], np.int32))
+        self.w = w
+        nkv, hd, bs = w.num_kv_heads, w.head_dim, w.block_size
+        self.tables = W.block_tables(w)
+        slots = W.slot_mapping_for_sequences(w, self.tables)
+        kside, vside = oracle.kv_pair(fmt)
+        self.kst = oracle.block_bytes(kside, bs, nkv, hd)
+        self.vst = oracle.block_bytes(vside, bs, nkv, hd)
+        self.kc = np.zeros(w.num_blocks * self.kst, np.uint8)
+        self.vc = np.zeros(w.num_blocks * self.vst, np.uint8)
+        oracle.cache_write(kside, W.kv_rows(w, 0, ntok), self.kc, slots, nkv, hd, bs, self.kst)
+        oracle.cache_write(vside, W.kv_rows(w, 1, ntok), self.vc, slots, nkv, hd, bs, self.vst)
+        self.q = W.q_rows(w)
+        self.nbytes = ntok * (self.kst + self.vst) // bs
+        self.desc = (f"one {fmt} sequence of the workload ({ntok} tokens, 8 kv / 32 q heads, "
+                     f"{self.nbytes} cache bytes) decoded by the numpy oracle")
+
+    def run(self):
+        w = self.w
+        self.oracle.paged_decode(self.q, self.kc, self.vc, self.tables, w.seq_lens,
+                                 w.num_kv_heads, w.head_dim, w.block_size, self.kst, self.vst,
+                                 self.fmt)
+
+
+def cpu_baseline(seconds=15.0):
+    s = OracleSample(4096)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        s.run()
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": round(done * s.nbytes / el / 1e9, 4), "unit": "GB/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done} x {s.desc} in {el:.1f} s; numpy BLAS threads at their default "
+                      "(all cores)"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    s = OracleSample(512)
+    for _ in range(args.warmup):
+        s.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s.run()
+    el = time.perf_counter() - t0
+    v = args.steps * s.nbytes / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama8b decode layer (turbo4 layer), each step a 512-token "
+                                   "sample of one sequence", "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": f"{args.steps} x {s.desc}"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,23 @@
+// Decode instances whose K side is T2 (one translation unit per K side
+// so the instances compile in parallel).  V sides: the catalogue's pairs
+// with this K side ("spark_runtime/kv_cache.rs", KvCacheDtype::kv_pair).
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+cudaError_t launch_decode_k_t2(int v_side, int hd, int rmax, const DecodeArgs& a,
+                                 const Codebooks& cb, cudaStream_t st) {
+  switch (v_side) {
+    case S_T2: return launch_decode_pair<S_T2, S_T2>(hd, rmax, a, cb, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+size_t smem_k_t2(int v_side, int hd, int rmax) {
+  switch (v_side) {
+    case S_T2: return smem_pair<S_T2, S_T2>(hd, rmax);
+    default: return 0;
+  }
+}
+
+}  // namespace kvq

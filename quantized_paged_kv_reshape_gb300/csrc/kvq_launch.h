@@ -1,0 +1,94 @@
+// Argument blocks and launchers shared between the C ABI (kvq_api.cpp) and
+// the kernel translation units.  Host-validated values only: the kernels
+// trust these fields.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvq {
+
+struct Codebooks;
+
+struct WriteArgs {
+  const void* key;
+  const void* value;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  const int64_t* slots;
+  int32_t num_tokens;
+  int64_t num_slots;      // num_blocks * block_size, 0 = unchecked
+  int32_t nkv;
+  int32_t bs;
+  int64_t key_stride, value_stride;     // elements per token
+  int64_t k_bstride, v_bstride;         // bytes per block
+  int64_t k_dsec, v_dsec;               // scale-section offsets
+  float k_scale, v_scale;               // per-tensor FP8 scales
+  float inv_sqrt_hd;                    // fp32(1/sqrt(head_dim))
+  int k_side, v_side;
+  int32_t* err;
+};
+
+struct DecodeArgs {
+  const void* q;
+  int64_t q_stride;       // elements between sequences
+  int q_bf16;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  int32_t num_seqs;
+  int64_t num_blocks;     // 0 = unchecked
+  int32_t nq, nkv, rep;   // rep = nq / nkv
+  int32_t bs;
+  int64_t k_bstride, v_bstride, k_dsec, v_dsec;
+  float score_scale;      // sm_scale * log2(e) (* k_scale for FP8 K)
+  float v_mult;           // v_scale for FP8 V, else 1
+  float inv_sqrt_hd;
+  int32_t window;
+  float sparse_thr;
+  int32_t pages_per_split;
+  int32_t nsplit;
+  float* part;            // [num_seqs][nq][nsplit][head_dim + 4] fp32
+  int32_t* err;
+};
+
+struct CombineArgs {
+  const float* part;
+  void* out;
+  int out_bf16;
+  int32_t num_seqs, nq, nsplit;
+  int v_rotated;
+  float inv_sqrt_hd;
+};
+
+cudaError_t launch_cache_write(const WriteArgs& a, const Codebooks& cb, int head_dim,
+                               bool in_bf16, bool vec, int grid, cudaStream_t st);
+
+// Split-K decode for one (K side, V side) pair; returns cudaErrorInvalidValue
+// for a pair / head_dim / rmax without an instance.
+cudaError_t launch_decode(int k_side, int v_side, int head_dim, int rmax,
+                          const DecodeArgs& a, const Codebooks& cb, cudaStream_t st);
+
+cudaError_t launch_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
+
+// Per-K-side entry points, one translation unit each.
+cudaError_t launch_decode_k_bf16(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_decode_k_fp8(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_decode_k_t4(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_decode_k_t3(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_decode_k_t2(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_decode_k_t8(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
+size_t smem_k_bf16(int v_side, int hd, int rmax);
+size_t smem_k_fp8(int v_side, int hd, int rmax);
+size_t smem_k_t4(int v_side, int hd, int rmax);
+size_t smem_k_t3(int v_side, int hd, int rmax);
+size_t smem_k_t2(int v_side, int hd, int rmax);
+size_t smem_k_t8(int v_side, int hd, int rmax);
+
+
+// Shared memory bytes the decode instance needs (0 if no instance).
+size_t decode_smem_bytes(int k_side, int v_side, int head_dim, int rmax);
+
+}  // namespace kvq

@@ -1,0 +1,254 @@
+// Cache-write kernel: scatter K/V rows into the paged cache, each side in its
+// own storage format, both sides in one launch.
+//
+// "metrale_model_layers/layers/ops/kv_cache_bf16k_turbov.rs",
+// reshape_and_cache_bf16k_turbo{2,3,4}v (arguments: key/value with per-token
+// element strides, slot_mapping, k/v block strides in bytes, the V data
+// section size); "spark_runtime/kv_cache.rs", KvCacheDtype::Turbo4KTurbo3V
+// (one launch forks the K-side and V-side writers) and the Turbo2/3/4/8, Fp8
+// and Bf16 storage descriptions.
+//
+// Work mapping: one warp per (token, kv head, side) row; lane l holds the E =
+// head_dim/32 consecutive elements l*E .. l*E+E-1.  The rotation runs in
+// registers and warp shuffles, the 16-element group max in a shuffle
+// reduction over the 16/E lanes of the group, the codes are packed per lane
+// and merged across the few lanes whose bits complete a byte, then stored.
+// Rows of consecutive warps are consecutive kv heads of one token, so both
+// the strided input reads and the cache stores of a token are contiguous.
+#include "kvq_common.cuh"
+#include "kvq_launch.h"
+
+namespace kvq {
+
+namespace {
+
+template <int N>
+__device__ __forceinline__ void store_bytes(uint8_t* dst, uint32_t lo, uint32_t hi = 0) {
+  if constexpr (N == 1) {
+    *dst = (uint8_t)lo;
+  } else if constexpr (N == 2) {
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)lo;
+  } else if constexpr (N == 3) {
+    dst[0] = (uint8_t)lo;
+    dst[1] = (uint8_t)(lo >> 8);
+    dst[2] = (uint8_t)(lo >> 16);
+  } else if constexpr (N == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = lo;
+  } else if constexpr (N == 8) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+  }
+}
+
+template <int E, typename InT, bool VEC>
+__device__ __forceinline__ void load_row(const InT* src, float (&x)[E]) {
+  if constexpr (VEC && sizeof(InT) == 2) {
+    // E bf16 = 2E bytes: 4, 8 or 16 byte vector loads
+    if constexpr (E == 2) {
+      uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(src));
+      x[0] = bf16_bits_to_float(w & 0xffffu);
+      x[1] = bf16_bits_to_float(w >> 16);
+    } else if constexpr (E == 4) {
+      uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+      x[0] = bf16_bits_to_float(w.x & 0xffffu); x[1] = bf16_bits_to_float(w.x >> 16);
+      x[2] = bf16_bits_to_float(w.y & 0xffffu); x[3] = bf16_bits_to_float(w.y >> 16);
+    } else {
+      uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = bf16_bits_to_float(ws[i] & 0xffffu);
+        x[2 * i + 1] = bf16_bits_to_float(ws[i] >> 16);
+      }
+    }
+  } else if constexpr (VEC && sizeof(InT) == 4) {
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      float2 f = __ldg(reinterpret_cast<const float2*>(src) + i / 2);
+      x[i] = f.x;
+      x[i + 1] = f.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      if constexpr (sizeof(InT) == 2)
+        x[i] = bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(src) + i));
+      else
+        x[i] = __ldg(reinterpret_cast<const float*>(src) + i);
+    }
+  }
+}
+
+// Pack E codes of B bits (code i at bits B*i) and store the row's code bytes:
+// lanes whose bits do not fill whole bytes are merged into a chunk of C lanes
+// first (C*B*E bits, a whole number of bytes <= 4).
+template <int B, int E>
+__device__ __forceinline__ void store_codes(uint8_t* row_codes, const int (&code)[E], int lane) {
+  constexpr int LB = B * E;                       // bits per lane
+  constexpr int G = (LB % 8 == 0) ? 8 : (LB % 4 == 0) ? 4 : 2;  // gcd(LB, 8)
+  constexpr int C = 8 / G;                        // lanes per whole-byte chunk
+  constexpr int CB = C * LB / 8;                  // bytes per chunk
+  static_assert(C * LB <= 32, "chunk exceeds 32 bits");
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < E; ++i) bits |= (uint32_t)code[i] << (B * i);
+#pragma unroll
+  for (int j = 1; j < C; ++j) {
+    uint32_t o = __shfl_down_sync(0xffffffffu, bits, j);
+    if ((lane % C) == 0) bits |= o << (j * LB);
+  }
+  if ((lane % C) == 0) store_bytes<CB>(row_codes + (lane / C) * CB, bits);
+}
+
+template <int E>
+__device__ __forceinline__ float group_amax(const float (&y)[E]) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) a = fmaxf(a, fabsf(y[i]));
+  constexpr int LPG = kGroup / E;  // lanes per group
+#pragma unroll
+  for (int m = 1; m < LPG; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  return a;
+}
+
+template <int HD, int B>
+__device__ __forceinline__ void write_turbo(float (&y)[HD / 32], const float lv_max,
+                                            const float (&th)[(1 << B) - 1], uint8_t* row_codes,
+                                            uint8_t* row_scales, int lane) {
+  constexpr int E = HD / 32;
+  const float amax = group_amax<E>(y);
+  const float ratio = amax / lv_max;               // IEEE fp32 divide
+  const uint8_t sbyte = e4m3_from_float(ratio);
+  const float s = e4m3_to_float(sbyte);
+  int code[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    if (s == 0.f) {
+      code[i] = 1 << (B - 1);
+    } else {
+      const float v = y[i] / s;                     // IEEE fp32 divide
+      code[i] = B == 4 ? lm_code4(v, th) : B == 3 ? lm_code3(v, th) : lm_code2(v, th);
+    }
+  }
+  store_codes<B, E>(row_codes, code, lane);
+  constexpr int LPG = kGroup / E;
+  if ((lane % LPG) == 0) row_scales[lane / LPG] = sbyte;
+}
+
+template <int HD, typename InT, bool VEC>
+__global__ void __launch_bounds__(256)
+cache_write_kernel(const WriteArgs a, const Codebooks cb) {
+  constexpr int E = HD / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t rows = (int64_t)a.num_tokens * a.nkv * 2;
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps_total) {
+    const int64_t t = row / (2 * a.nkv);
+    const int rem = (int)(row - t * 2 * a.nkv);
+    const int side = rem >= a.nkv;
+    const int h = rem - side * a.nkv;
+    const int64_t slot = a.slots[t];
+    if (slot < 0) continue;
+    if (a.num_slots > 0 && slot >= a.num_slots) {
+      if (lane == 0 && a.err) atomicOr(a.err, 1);
+      continue;
+    }
+    const int64_t blk = slot / a.bs;
+    const int off = (int)(slot - blk * a.bs);
+    const int fmt = side ? a.v_side : a.k_side;
+    const InT* src = reinterpret_cast<const InT*>(side ? a.value : a.key) +
+                     t * (side ? a.value_stride : a.key_stride) + (int64_t)h * HD + lane * E;
+    uint8_t* base = (side ? a.v_cache : a.k_cache) + blk * (side ? a.v_bstride : a.k_bstride);
+    const int64_t dsec = side ? a.v_dsec : a.k_dsec;
+    const int64_t ridx = (int64_t)off * a.nkv + h;   // row index inside the block
+
+    float x[E];
+    load_row<E, InT, VEC>(src, x);
+
+    if (fmt == S_BF16) {
+      uint32_t w[(E + 1) / 2];
+#pragma unroll
+      for (int i = 0; i < E; i += 2)
+        w[i / 2] = (uint32_t)bf16_bits_from_float(x[i]) |
+                   ((uint32_t)bf16_bits_from_float(x[i + 1]) << 16);
+      uint8_t* dst = base + (ridx * HD + lane * E) * 2;
+      if constexpr (E == 2) store_bytes<4>(dst, w[0]);
+      else if constexpr (E == 4) store_bytes<8>(dst, w[0], w[1]);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (fmt == S_FP8) {
+      const float sc = side ? a.v_scale : a.k_scale;
+      uint32_t w[(E + 3) / 4] = {};
+#pragma unroll
+      for (int i = 0; i < E; ++i) w[i / 4] |= (uint32_t)e4m3_from_float(x[i] / sc) << (8 * (i % 4));
+      uint8_t* dst = base + ridx * HD + lane * E;
+      if constexpr (E == 2) store_bytes<2>(dst, w[0]);
+      else if constexpr (E == 4) store_bytes<4>(dst, w[0]);
+      else store_bytes<8>(dst, w[0], w[1]);
+    } else {
+      fwht_warp<E>(x, lane, a.inv_sqrt_hd);
+      if (fmt == S_T8) {
+        const float amax = group_amax<E>(x);
+        const uint16_t sbits = bf16_bits_from_float(amax / 448.0f);
+        const float s = bf16_bits_to_float(sbits);
+        uint32_t w[(E + 3) / 4] = {};
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const uint32_t b = s == 0.f ? 0u : (uint32_t)e4m3_from_float(x[i] / s);
+          w[i / 4] |= b << (8 * (i % 4));
+        }
+        uint8_t* dst = base + ridx * HD + lane * E;
+        if constexpr (E == 2) store_bytes<2>(dst, w[0]);
+        else if constexpr (E == 4) store_bytes<4>(dst, w[0]);
+        else store_bytes<8>(dst, w[0], w[1]);
+        constexpr int LPG = kGroup / E;
+        if ((lane % LPG) == 0)
+          store_bytes<2>(base + dsec + (ridx * (HD / kGroup) + lane / LPG) * 2, sbits);
+      } else if (fmt == S_T4) {
+        float th[15];
+#pragma unroll
+        for (int i = 0; i < 15; ++i) th[i] = cb.th4[i];
+        write_turbo<HD, 4>(x, cb.lv4[15], th, base + ridx * (HD / 2),
+                           base + dsec + ridx * (HD / kGroup), lane);
+      } else if (fmt == S_T3) {
+        float th[7];
+#pragma unroll
+        for (int i = 0; i < 7; ++i) th[i] = cb.th3[i];
+        write_turbo<HD, 3>(x, cb.lv3[7], th, base + ridx * (HD * 3 / 8),
+                           base + dsec + ridx * (HD / kGroup), lane);
+      } else {
+        float th[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) th[i] = cb.th2[i];
+        write_turbo<HD, 2>(x, cb.lv2[3], th, base + ridx * (HD / 4),
+                           base + dsec + ridx * (HD / kGroup), lane);
+      }
+    }
+  }
+}
+
+template <int HD, typename InT>
+cudaError_t launch_hd(const WriteArgs& a, const Codebooks& cb, bool vec, int grid,
+                      cudaStream_t st) {
+  if (vec)
+    cache_write_kernel<HD, InT, true><<<grid, 256, 0, st>>>(a, cb);
+  else
+    cache_write_kernel<HD, InT, false><<<grid, 256, 0, st>>>(a, cb);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_cache_write(const WriteArgs& a, const Codebooks& cb, int head_dim,
+                               bool in_bf16, bool vec, int grid, cudaStream_t st) {
+  switch (head_dim) {
+    case 64: return in_bf16 ? launch_hd<64, __nv_bfloat16>(a, cb, vec, grid, st)
+                            : launch_hd<64, float>(a, cb, vec, grid, st);
+    case 128: return in_bf16 ? launch_hd<128, __nv_bfloat16>(a, cb, vec, grid, st)
+                             : launch_hd<128, float>(a, cb, vec, grid, st);
+    case 256: return in_bf16 ? launch_hd<256, __nv_bfloat16>(a, cb, vec, grid, st)
+                             : launch_hd<256, float>(a, cb, vec, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

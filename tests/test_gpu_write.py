@@ -1,0 +1,89 @@
+"""GPU cache write vs the oracle: stored code and scale bytes bit-exact.
+
+Every catalogue format (both sides in one launch), head_dim 64/128/256,
+fp32 and bf16 activations, K/V read through fused-QKV strides, a ragged
+token count with skipped (-1) slots, padded block strides, and a slot past
+the pool that must be flagged instead of written."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_paged_kv_reshape_gb300 import ops
+from kvq_cases import ALL_FORMATS, bf16_round, fp8_scales
+
+pytestmark = pytest.mark.gpu
+
+
+def run_write(fmt, hd, in_dtype, nkv=2, bs=16, num_blocks=7, ntok=45, seed=0, pad=32,
+              bad_slot=False):
+    rng = np.random.default_rng(seed)
+    nq = 2 * nkv
+    row = (nq + 2 * nkv) * hd + 8           # fused QKV row, stride != nkv*hd
+    fused = rng.standard_normal((ntok, row)).astype(np.float32)
+    fused[:, rng.choice(row, 6, replace=False)] *= 10.0      # outlier channels
+    fused[3, :] = 0.0                                         # an all-zero token
+    if in_dtype == "bf16":
+        fused = bf16_round(fused)
+    slots = rng.permutation(num_blocks * bs)[:ntok].astype(np.int64)
+    slots[rng.choice(ntok, 5, replace=False)] = -1
+    if bad_slot:
+        slots[7] = num_blocks * bs + 3
+    koff, voff = nq * hd, (nq + nkv) * hd
+    kview = fused[:, koff:koff + nkv * hd].reshape(ntok, nkv, hd)
+    vview = fused[:, voff:voff + nkv * hd].reshape(ntok, nkv, hd)
+    kside, vside = oracle.kv_pair(fmt)
+    ks, vs = fp8_scales(kview, vview)
+    kst = (oracle.block_bytes(kside, bs, nkv, hd) + 15) // 16 * 16 + pad
+    vst = (oracle.block_bytes(vside, bs, nkv, hd) + 15) // 16 * 16 + pad
+    kc = np.zeros(num_blocks * kst, np.uint8)
+    vc = np.zeros(num_blocks * vst, np.uint8)
+    ok_slots = np.where(slots < num_blocks * bs, slots, -1)
+    oracle.cache_write(kside, kview, kc, ok_slots, nkv, hd, bs, kst, scale=ks)
+    oracle.cache_write(vside, vview, vc, ok_slots, nkv, hd, bs, vst, scale=vs)
+
+    dev = "cuda"
+    tdt = torch.bfloat16 if in_dtype == "bf16" else torch.float32
+    fused_d = torch.from_numpy(fused).to(dev).to(tdt)
+    kpool = torch.zeros((num_blocks, kst), dtype=torch.uint8, device=dev)
+    vpool = torch.zeros((num_blocks, vst), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ops.cache_write(fused_d[:, koff:], fused_d[:, voff:], kpool, vpool,
+                    torch.from_numpy(slots).to(dev), fmt, nkv, hd, bs, key_stride=row,
+                    value_stride=row, k_scale=ks, v_scale=vs, error_flag=err)
+    torch.cuda.synchronize()
+    return kc, vc, kpool.cpu().numpy().reshape(-1), vpool.cpu().numpy().reshape(-1), int(err.item())
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hd", [64, 128, 256])
+@pytest.mark.parametrize("fmt", ALL_FORMATS)
+def test_write_bit_exact(fmt, hd, in_dtype):
+    kc, vc, kg, vg, err = run_write(fmt, hd, in_dtype, seed=hd)
+    assert err == 0
+    assert np.array_equal(kc, kg), f"K bytes differ at {np.flatnonzero(kc != kg)[:8]}"
+    assert np.array_equal(vc, vg), f"V bytes differ at {np.flatnonzero(vc != vg)[:8]}"
+
+
+@pytest.mark.parametrize("fmt", ["turbo4", "bf16k_turbo3v", "fp8k_turbo2v", "turbo8"])
+def test_write_flags_slot_past_pool(fmt):
+    kc, vc, kg, vg, err = run_write(fmt, 128, "bf16", bad_slot=True)
+    assert err & 1
+    assert np.array_equal(kc, kg) and np.array_equal(vc, vg)
+
+
+@pytest.mark.parametrize("nkv,bs", [(1, 8), (3, 16), (16, 32)])
+def test_write_shapes(nkv, bs):
+    for fmt in ("turbo3", "turbo2", "fp8k_turbo4v"):
+        kc, vc, kg, vg, err = run_write(fmt, 128, "bf16", nkv=nkv, bs=bs, num_blocks=9, ntok=60)
+        assert np.array_equal(kc, kg) and np.array_equal(vc, vg)
+
+
+def test_write_empty_is_noop():
+    dev = "cuda"
+    kpool = torch.zeros((2, 4096), dtype=torch.uint8, device=dev)
+    x = torch.zeros((1, 256), dtype=torch.bfloat16, device=dev)
+    ops.cache_write(x, x, kpool, kpool, torch.zeros(0, dtype=torch.int64, device=dev),
+                    "turbo4", 2, 128, 16)
+    torch.cuda.synchronize()
+    assert not kpool.any()
