@@ -63,9 +63,11 @@ def test_decode_long_sequence_many_splits():
 
 
 def test_sparse_v_reported():
-    """Sparse-V is approximate: the kernel drops weights <= 1e-3 of their
-    split's running sum, the oracle <= 1e-3 of the global sum.  Checked: both
-    stay close to the exact output; the difference is reported."""
+    """Sparse-V is approximate and not parity-gated: the kernel drops weights
+    <= 1e-3 of their split's running sum (never more than the oracle, which
+    drops weights <= 1e-3 of the global sum).  Checked: the kernel's error
+    against the exact output is finite and not above the oracle's own
+    sparse-V error; both are printed."""
     c = decode_case("fp8k_turbo2v", [400, 1000], 32, 8, 128, seed=5)
     exact = oracle_decode(c)
     got = gpu_decode(c, sparse=1e-3)
@@ -73,7 +75,8 @@ def test_sparse_v_reported():
     e_gpu = np.abs(got - exact).max()
     e_ref = np.abs(ref - exact).max()
     print(f"sparse-V 1e-3: kernel vs exact max-abs {e_gpu:.3e}, oracle vs exact {e_ref:.3e}")
-    assert e_gpu < 0.1 and e_ref < 0.1
+    assert np.isfinite(got).all()
+    assert e_gpu <= e_ref + 1e-3
 
 
 def test_decode_flags_bad_block():
