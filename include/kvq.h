@@ -30,7 +30,8 @@
  * Conventions shared by every call:
  *   - All device pointers are plain CUDA device addresses owned by the
  *     caller; the library allocates nothing and keeps no state between
- *     calls except the host-side codebook tables, built once per process.
+ *     calls except the host-side codebook tables, built once per process,
+ *     and the fixed scratch array of kvq_paged_decode_noalloc.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls only enqueue work; none synchronizes the host.
  *   - Errors are returned as kvq_status; arguments are validated on the host
@@ -147,7 +148,7 @@ const char* kvq_last_error(void);
 /* ------------------------------------------------------------- cache write */
 
 /* [METRALE] reshape_and_cache_bf16k_turbo{2,3,4}v; [ATLAS] Turbo4KTurbo3V
- * ("the write kernel forks ... for K and ... for V on the same launch").
+ * (one launch writes the K side and the V side, each in its own format).
  *
  * For each token t < num_tokens with slot = slot_mapping[t] >= 0, and each
  * kv head h, row (t, h) of `key` (resp. `value`) - the head_dim elements
@@ -232,6 +233,42 @@ kvq_status kvq_paged_decode(
     float sm_scale, float k_scale, float v_scale,
     int32_t sliding_window, float sparse_v_threshold,
     void* workspace, size_t workspace_bytes, kvq_format fmt,
+    int32_t* error_flag, void* stream);
+
+/* -------------------------------------------- decode without an allocation */
+
+/* Bytes of the scratch array built into the library for
+ * kvq_paged_decode_noalloc (per GPU that loads the library, kept until the
+ * process exits). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory - a runtime that has already given all
+ * device memory to its own pool, a plugin host that forbids plugins from
+ * allocating, or a latency-critical loop where cudaMalloc's possible device
+ * synchronization is not acceptable.
+ *
+ * Same arguments and results as kvq_paged_decode, minus the workspace: the
+ * split-K partials go to a fixed KVQ_NOALLOC_SCRATCH_BYTES array compiled
+ * into the library.  Nothing is allocated (no cudaMalloc / cudaFree).
+ *   - Returns KVQ_ERR_WORKSPACE if kvq_decode_workspace_bytes(...) for these
+ *     arguments exceeds KVQ_NOALLOC_SCRATCH_BYTES.
+ *   - The first call with a given device current looks the array's device
+ *     address up (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array: calls whose kernels overlap on the GPU
+ *     (different streams, or different host threads) race.  Serialize them. */
+kvq_status kvq_paged_decode_noalloc(
+    const void* q, kvq_dtype q_dtype, int64_t q_stride,
+    const void* k_cache, const void* v_cache,
+    void* out, kvq_dtype out_dtype,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens, int32_t num_seqs, int64_t num_blocks,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size,
+    int64_t k_block_stride_bytes, int64_t v_block_stride_bytes,
+    float sm_scale, float k_scale, float v_scale,
+    int32_t sliding_window, float sparse_v_threshold, kvq_format fmt,
     int32_t* error_flag, void* stream);
 
 #ifdef __cplusplus

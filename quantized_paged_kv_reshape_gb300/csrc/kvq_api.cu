@@ -184,6 +184,10 @@ size_t decode_smem(int ks, int vs, int hd, int rmax) {
 }  // namespace
 
 namespace kvq {
+// Lets other translation units of the library report a message through
+// kvq_last_error().
+void record_error(const char* msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
+
 size_t decode_smem_bytes(int k_side, int v_side, int head_dim, int rmax) {
   return decode_smem(k_side, v_side, head_dim, rmax);
 }

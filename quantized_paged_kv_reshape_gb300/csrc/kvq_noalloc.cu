@@ -1,0 +1,86 @@
+// Paged decode for callers that cannot allocate device memory.
+//
+// kvq_paged_decode needs a caller-provided scratch buffer for its split-K
+// partial results.  Some callers cannot get one: a runtime that has already
+// handed all device memory to its own pool, a plugin host that forbids
+// device allocations by its plugins, or a latency-critical loop where
+// cudaMalloc (which may synchronize the device) is not acceptable.  This
+// entry point runs the same kernels with the scratch taken from a fixed
+// array compiled into the library instead; it allocates nothing.
+//
+// The array lives in every GPU that loads the library, for the life of the
+// process.  Host code must not use the array's name as a device address (on
+// the host it only names a stand-in); the device address is looked up with
+// cudaGetSymbolAddress once per device, on the first call made with that
+// device current, and cached.  Make that first call before any stream
+// capture.  All calls share the one array and the decode leaves its
+// partials there, so calls whose kernels overlap on the GPU race; the
+// decode writes every partial before reading it, so nothing needs clearing.
+#include "../../include/kvq.h"
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+namespace kvq {
+void record_error(const char* msg);
+}
+
+namespace {
+
+constexpr size_t kScratchBytes = KVQ_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+kvq_status scratch_for_current_device(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    kvq::record_error("no usable current CUDA device for the built-in decode scratch");
+    return KVQ_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || !p) {
+      kvq::record_error("cudaGetSymbolAddress of the built-in decode scratch failed");
+      return KVQ_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_paged_decode_noalloc(
+    const void* q, kvq_dtype q_dtype, int64_t q_stride, const void* k_cache, const void* v_cache,
+    void* out, kvq_dtype out_dtype, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens, int32_t num_seqs, int64_t num_blocks, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t k_block_stride_bytes,
+    int64_t v_block_stride_bytes, float sm_scale, float k_scale, float v_scale,
+    int32_t sliding_window, float sparse_v_threshold, kvq_format fmt, int32_t* error_flag,
+    void* stream) {
+  const size_t need = kvq_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 block_size, max_blocks_per_seq, sliding_window,
+                                                 fmt);
+  if (need > kScratchBytes) {
+    kvq::record_error(
+        "decode needs more scratch than the built-in 8 MiB (fewer sequences or heads per call, "
+        "or kvq_paged_decode with a caller-provided workspace)");
+    return KVQ_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  const kvq_status st = scratch_for_current_device(&scratch);
+  if (st != KVQ_OK) return st;
+  return kvq_paged_decode(q, q_dtype, q_stride, k_cache, v_cache, out, out_dtype, block_tables,
+                          max_blocks_per_seq, seq_lens, num_seqs, num_blocks, num_q_heads,
+                          num_kv_heads, head_dim, block_size, k_block_stride_bytes,
+                          v_block_stride_bytes, sm_scale, k_scale, v_scale, sliding_window,
+                          sparse_v_threshold, scratch, kScratchBytes, fmt, error_flag, stream);
+}
