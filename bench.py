@@ -136,6 +136,9 @@ def run_gpu(args):
     _abi.lib()
 
     w = W.make(WORKLOAD, seed=rank)
+    if args.num_seqs != w.num_seqs:
+        w = W.make(WORKLOAD, seed=rank, num_seqs=args.num_seqs,
+                   seq_lens=np.full(args.num_seqs, int(w.seq_lens[0]), np.int32))
     nkv, nq, hd, bs = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size
     nseq = w.num_seqs
     L = int(w.seq_lens[0])
@@ -157,7 +160,7 @@ def run_gpu(args):
     k_scale = float(kall.float().abs().amax()) / 448.0
     v_scale = float(vall.float().abs().amax()) / 448.0
 
-    fmts = list(w.formats)
+    fmts = [f for f in w.formats if f in args.formats.split(",")] if args.formats else list(w.formats)
     pools = {}
     write_ms = {}
     for f in fmts:
@@ -284,15 +287,16 @@ def run_gpu(args):
     dom = max(fmts, key=lambda f: per_fmt[f]["us_per_layer"])
     value = step_bytes * ws / (ms_step * 1e-3) / 1e9
     e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
-    launches_per_step = 3 * len(fmts)   # write + decode split + combine per format
+    launches_per_step = 3 * len(fmts)   # noqa: E501   # write + decode split + combine per format
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "llama8b decode layer: 32 seqs x 4096 ctx, 32 q / 8 kv heads, "
-                               "head_dim 128, block_size 16; one layer per format bf16, fp8, turbo4",
-                   "formats": fmts, "l2": "inputs larger than L2 (956 MB of cache per step)",
+        "config": {"workload": f"llama8b decode layer: {nseq} seqs x {L} ctx, 32 q / 8 kv heads, "
+                               "head_dim 128, block_size 16; one layer per format",
+                   "formats": fmts,
+                   "l2": f"inputs larger than L2 ({sum(dec_bytes.values()) / 1e6:.0f} MB of cache per step)",
                    "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
         "per_format": per_fmt,
         "roofline": {"kernel": f"decode_split_kernel ({dom})", "bound": "hbm",
@@ -395,6 +399,8 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=32, help="sequences of 4096 tokens")
+    ap.add_argument("--formats", default="", help="comma list (default bf16,fp8,turbo4)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -161,6 +161,7 @@ SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, 
   ns = std::min(std::max<int64_t>(ns, 1), max_ns);
   int pps = (int)((pages + ns - 1) / ns);
   pps = (pps + tp - 1) / tp * tp;
+  if (pps > 512) pps = 512;  // the tensor-core kernel stages a split's block ids in smem
   const int nsplit = (pages + pps - 1) / pps;
   return {nsplit, pps};
 }
@@ -419,7 +420,8 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   a.part = (float*)workspace;
   a.err = error_flag;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_decode(ks, vs, hd, rmax, a, cb, st);
+  cudaError_t e = decode_tc_supported(ks, vs) ? launch_decode_tc(ks, vs, hd, a, st)
+                                               : launch_decode(ks, vs, hd, rmax, a, cb, st);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   CombineArgs c{};
   c.part = a.part;

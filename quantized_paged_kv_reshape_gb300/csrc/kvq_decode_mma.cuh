@@ -1,0 +1,503 @@
+// Split-K paged decode with the GQA contraction on tensor cores.
+//
+// Same result as decode_split_kernel ("combs_models/kv.rs" attend + repeat_kv
+// for one query over the pages of the block tables; "spark_runtime/
+// kv_cache.rs" is_wht_rotated bookends), for sides whose stored values are
+// exact in a 16-bit MMA operand: BF16 (bf16 operands) and FP8 E4M3 (fp16
+// operands; the per-tensor scale is applied to the fp32 results).
+//
+// Per warp and per slab of 16 token positions:
+//   S^T[16 tok x 8 q-heads] = K[16 x hd] . Q^T[hd x 8]      (m16n8k16, hd/16 steps)
+//   online softmax on the fp32 accumulators (exp2 domain)
+//   O^T[hd x 8] += V^T[hd x 16 tok] . P^T[16 x 8]           (hd/16 m-tiles)
+// The query and P operands are split into hi + lo 16-bit parts (two MMAs
+// each), so the products carry ~16 significant bits: a single 16-bit pass
+// misses the 2e-3 output bound on outlier-heavy inputs.  K and V values are
+// exact in the operand type, so they need no split.  P^T's operand
+// fragments come from the S accumulators by an in-register 8x8 transpose
+// (movmatrix).  BF16 rows go to the MMAs through ldmatrix (.trans for V);
+// FP8 rows are converted in registers: K's reduction dimension is permuted
+// per thread so that each thread converts whole 16-byte chunks (q uses the
+// same permutation), and V's E4M3 bytes of two tokens are byte-interleaved
+// (prmt) before the e4m3x2 -> f16x2 conversion, with the output dims of the
+// fragments permuted accordingly.
+//
+// Each warp owns a private cp.async ring of slabs (no CTA barrier inside the
+// loop); the 4 warps of a CTA take slabs w, w+4, ... of the split and are
+// merged through shared memory at the end.  Positions outside [lo, L), past
+// the split or with a bad block id are zero-filled and masked to -inf.
+#pragma once
+
+#include <math_constants.h>
+
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+namespace tc {
+
+template <bool BF>
+__device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                    uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(s));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(s));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// (lo, hi) -> packed 16-bit pair, round to nearest even.
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t r;
+  if constexpr (BF)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+template <bool BF>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if constexpr (BF) {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  } else {
+    __half2_raw h;
+    h.x = (unsigned short)(v & 0xffffu);
+    h.y = (unsigned short)(v >> 16);
+    return __half22float2(__half2(h));
+  }
+}
+// x = hi + lo with hi, lo 16-bit: ~16 significant bits in total.
+template <bool BF>
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack2<BF>(x0, x1);
+  const float2 h = unpack2<BF>(hi);
+  lo = pack2<BF>(x0 - h.x, x1 - h.y);
+}
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t lo16) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"((unsigned short)lo16));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+}  // namespace tc
+
+// Per-side layout of the staged rows of one slab (16 positions).
+template <int S, int HD>
+struct TcSide {
+  static constexpr bool BF = S == S_BF16;
+  static constexpr int ROW = SideGeom<S, HD>::ROW;
+  // K rows: ldmatrix wants 8 rows at distinct 16-byte bank groups (stride
+  // = 16 mod 128); FP8 K chunks want rows 2k, 2k+1 in opposite halves of
+  // the banks (stride = 64 mod 128).
+  static constexpr int KRS = BF ? ROW + 16 : (ROW % 128 == 0 ? ROW + 64 : ROW);
+  // V rows: ldmatrix.trans as above; FP8 V reads tokens 2c,2c+1,2c+8,2c+9.
+  static constexpr int VRS = BF ? ROW + 16 : (HD == 64 ? 80 : HD == 128 ? 144 : ROW + 16);
+};
+
+template <int KS, int VS, int HD>
+struct TcCfg {
+  using K = TcSide<KS, HD>;
+  using V = TcSide<VS, HD>;
+  static constexpr int NK = HD / 16;
+  static constexpr int STAGE = 16 * (K::KRS + V::VRS);
+  static constexpr int NST = (4 * 4 * STAGE <= 110 * 1024) ? 4 : (4 * 3 * STAGE <= 110 * 1024) ? 3 : 2;
+  static constexpr int MAXP = 512;                             // pages per split (host cap)
+  static constexpr int OFF_BLK = 8 * HD * 4;                   // after q_s [8][HD] fp32
+  static constexpr int OFF_OFFS = OFF_BLK + MAXP * 4;          // int32 block ids of the split
+  static constexpr int OFF_RING = OFF_OFFS + 4 * 32 * 8;       // per-warp row offsets
+  static constexpr int RING = 4 * NST * STAGE;
+  static constexpr int MERGE = 4 * 8 * HD * 4 + 4 * 8 * 2 * 4;
+  static constexpr int SMEM = OFF_RING + (RING > MERGE ? RING : MERGE);
+};
+
+// Dims carried by the B fragment of k-step j for thread c: b0b1 = (d, d+1),
+// b2b3 = (d+2, d+3) with d = kdim(j, c) (FP8: permuted), or
+// b0b1 = (d, d+1), b2b3 = (d+8, d+9) with d = 16j + 2c (BF16: natural).
+template <int S, int HD>
+__device__ __forceinline__ void k_slot_dims(int j, int c, int (&d)[4]) {
+  if constexpr (S == S_BF16) {
+    const int b = 16 * j + 2 * c;
+    d[0] = b; d[1] = b + 1; d[2] = b + 8; d[3] = b + 9;
+  } else {
+    const int b = 16 * (4 * (j / 4) + c) + 4 * (j % 4);
+    d[0] = b; d[1] = b + 1; d[2] = b + 2; d[3] = b + 3;
+  }
+}
+
+// Output dim of accumulator row `row` (0..15) of m-tile i.
+template <int S, int HD>
+__device__ __forceinline__ int v_row_dim(int i, int row) {
+  if constexpr (S == S_BF16) {
+    return 16 * i + row;
+  } else {
+    constexpr int DPT = HD / 8;  // dims per thread group g
+    return (row & 7) * DPT + 2 * i + (row >> 3);
+  }
+}
+
+template <int KS, int VS, int HD>
+__global__ void __launch_bounds__(128)
+decode_tc_kernel(const DecodeArgs a) {
+  using C = TcCfg<KS, VS, HD>;
+  using KT = typename C::K;
+  using VT = typename C::V;
+  constexpr int NK = C::NK;
+  constexpr int E = HD / 32;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* q_s = reinterpret_cast<float*>(smem);
+  uint8_t* rings = smem + C::OFF_RING;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int split = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  const int bs = a.bs;
+  const int L = a.seq_lens[seq];
+  const int lo = a.window > 0 ? max(0, L - a.window) : 0;
+  const int first_page = lo / bs;
+  int end_page = (L + bs - 1) / bs;
+  if (end_page > a.max_blocks) {
+    if (tid == 0 && split == 0 && a.err) atomicOr(a.err, 2);
+    end_page = a.max_blocks;
+  }
+  const int p0 = first_page + split * a.pages_per_split;
+  const int p1 = min(min(p0 + a.pages_per_split, end_page), p0 + C::MAXP);
+  const size_t pstride = (size_t)a.nsplit * (HD + 4);
+  float* part = a.part + ((size_t)(seq * a.nq + kvh * a.rep) * a.nsplit + split) * (HD + 4);
+  if (p0 >= p1) {
+    for (int j = warp; j < a.rep; j += 4)
+      for (int i = lane; i < HD + 4; i += 32) part[j * pstride + i] = (i == 0) ? -CUDART_INF_F : 0.f;
+    return;
+  }
+
+  // ---- queries (rotated when K is stored rotated), rows >= rep are zero
+  for (int j = warp; j < 8; j += 4) {
+    float x[E];
+    if (j < a.rep) {
+      const int64_t qoff = (int64_t)seq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        x[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
+                        : reinterpret_cast<const float*>(a.q)[qoff + i];
+      if constexpr (side_rotated(KS)) fwht_warp<E>(x, lane, a.inv_sqrt_hd);
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) x[i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) q_s[j * HD + lane * E + i] = x[i];
+  }
+  __syncthreads();
+  uint32_t qh[NK][2], ql[NK][2];
+#pragma unroll
+  for (int j = 0; j < NK; ++j) {
+    int d[4];
+    k_slot_dims<KS, HD>(j, c, d);
+    const float* qr = q_s + g * HD;
+    tc::split2<KT::BF>(qr[d[0]], qr[d[1]], qh[j][0], ql[j][0]);
+    tc::split2<KT::BF>(qr[d[2]], qr[d[3]], qh[j][1], ql[j][1]);
+  }
+
+  const int tok0 = p0 * bs;
+  const int tok_end = min(p1 * bs, L);
+  const int nslab = (tok_end - tok0 + 15) / 16;
+  const int my = nslab > warp ? (nslab - 1 - warp) / 4 + 1 : 0;
+  const int64_t tab = (int64_t)seq * a.max_blocks;
+  uint8_t* ring = rings + warp * C::NST * C::STAGE;
+  int* blk_s = reinterpret_cast<int*>(smem + C::OFF_BLK);
+  int64_t* offs = reinterpret_cast<int64_t*>(smem + C::OFF_OFFS) + warp * 32;
+  const int lbs = 31 - __clz(bs);  // block_size is a power of two
+
+  // Block ids of the split's pages, staged once (-1 = outside the pool).
+  for (int i = tid; i < p1 - p0; i += 128) {
+    const int64_t b = a.block_tables[tab + p0 + i];
+    const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
+    if (bad && a.err) atomicOr(a.err, 2);
+    blk_s[i] = bad ? -1 : (int)b;
+  }
+  __syncthreads();
+
+  // Block id of position pos, or -1 if it is not attended / not valid.
+  auto pos_block = [&](int pos) -> int {
+    if (pos < lo || pos >= tok_end) return -1;
+    return blk_s[(pos >> lbs) - p0];
+  };
+
+  // Row byte offsets of the slab (lanes 0-15: K row of position t = lane,
+  // lanes 16-31: V row), then 16-byte copies with consecutive lanes on
+  // consecutive chunks of the same row.
+  auto issue = [&](int s) {
+    uint8_t* sb = ring + (s % C::NST) * C::STAGE;
+    const int t = lane & 15;
+    const int pos = tok0 + (warp + 4 * s) * 16 + t;
+    const int b = pos_block(pos);
+    const int64_t ridx = (int64_t)(pos & (bs - 1)) * a.nkv + kvh;
+    offs[lane] = b < 0 ? -1
+                       : (lane < 16 ? (int64_t)b * a.k_bstride + ridx * KT::ROW
+                                    : (int64_t)b * a.v_bstride + ridx * VT::ROW);
+    __syncwarp();
+    constexpr int KC = KT::ROW / 16, VC = VT::ROW / 16;
+#pragma unroll
+    for (int q = lane; q < 16 * (KC + VC); q += 32) {
+      const bool isv = q >= 16 * KC;
+      const int q2 = isv ? q - 16 * KC : q;
+      const int row = isv ? q2 / VC : q2 / KC;
+      const int ch = isv ? q2 % VC : q2 % KC;
+      const int64_t off = offs[isv ? 16 + row : row];
+      const bool ok = off >= 0;
+      const uint8_t* src = (isv ? a.v_cache : a.k_cache) + (ok ? off : 0) + ch * 16;
+      uint8_t* dst = sb + (isv ? 16 * KT::KRS + row * VT::VRS : row * KT::KRS) + ch * 16;
+      cp_async<16>(dst, src, ok);
+    }
+  };
+
+#pragma unroll
+  for (int s = 0; s < C::NST - 1; ++s) {
+    if (s < my) issue(s);
+    cp_async_commit();
+  }
+
+  float o[NK][4];
+#pragma unroll
+  for (int i = 0; i < NK; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  const float scale = a.score_scale;
+
+  for (int s = 0; s < my; ++s) {
+    cp_async_wait<C::NST - 2>();
+    __syncwarp();
+    if (s + C::NST - 1 < my) issue(s + C::NST - 1);
+    cp_async_commit();
+    const uint8_t* sb = ring + (s % C::NST) * C::STAGE;
+    const uint8_t* kb = sb;
+    const uint8_t* vb = sb + 16 * KT::KRS;
+
+    // ---- S^T = K . Q^T
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (KS == S_BF16) {
+      const int mi = lane >> 3, rr = lane & 7;
+      const uint8_t* base = kb + ((mi & 1) * 8 + rr) * KT::KRS + (mi >> 1) * 16;
+#pragma unroll
+      for (int j = 0; j < NK; ++j) {
+        uint32_t f[4];
+        tc::ldsm_x4(f, base + j * 32);
+        tc::mma<true>(sacc, f[0], f[1], f[2], f[3], qh[j][0], qh[j][1]);
+        tc::mma<true>(sacc, f[0], f[1], f[2], f[3], ql[j][0], ql[j][1]);
+      }
+    } else {  // FP8: thread c converts 16-byte chunks 4jj + c of rows g and g+8
+#pragma unroll
+      for (int jj = 0; jj < NK / 4; ++jj) {
+        const uint4 ra = *reinterpret_cast<const uint4*>(kb + g * KT::KRS + (4 * jj + c) * 16);
+        const uint4 rb = *reinterpret_cast<const uint4*>(kb + (g + 8) * KT::KRS + (4 * jj + c) * 16);
+        const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
+        const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 4 * jj + e;
+          const uint32_t a0 = tc::e4m3x2_f16x2(wa[e] & 0xffffu), a4 = tc::e4m3x2_f16x2(wa[e] >> 16);
+          const uint32_t a2 = tc::e4m3x2_f16x2(wb[e] & 0xffffu), a6 = tc::e4m3x2_f16x2(wb[e] >> 16);
+          tc::mma<false>(sacc, a0, a2, a4, a6, qh[j][0], qh[j][1]);
+          tc::mma<false>(sacc, a0, a2, a4, a6, ql[j][0], ql[j][1]);
+        }
+      }
+    }
+
+    // ---- online softmax; this thread holds rows (tokens) g, g+8, cols 2c, 2c+1
+    const int slab_pos = tok0 + (warp + 4 * s) * 16;
+    const bool va = pos_block(slab_pos + g) >= 0;
+    const bool vb_ = pos_block(slab_pos + g + 8) >= 0;
+    const float s00 = va ? sacc[0] * scale : -CUDART_INF_F;
+    const float s01 = va ? sacc[1] * scale : -CUDART_INF_F;
+    const float s10 = vb_ ? sacc[2] * scale : -CUDART_INF_F;
+    const float s11 = vb_ ? sacc[3] * scale : -CUDART_INF_F;
+    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int msk = 4; msk < 32; msk <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, msk));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, msk));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    float al0 = 1.f, al1 = 1.f, p00 = 0.f, p10 = 0.f, p01 = 0.f, p11 = 0.f;
+    if (mn0 != -CUDART_INF_F) {
+      al0 = exp2f(m0 - mn0);
+      p00 = exp2f(s00 - mn0);
+      p10 = exp2f(s10 - mn0);
+    }
+    if (mn1 != -CUDART_INF_F) {
+      al1 = exp2f(m1 - mn1);
+      p01 = exp2f(s01 - mn1);
+      p11 = exp2f(s11 - mn1);
+    }
+    l0 = l0 * al0 + p00 + p10;
+    l1 = l1 * al1 + p01 + p11;
+    m0 = mn0;
+    m1 = mn1;
+    if (a.sparse_thr > 0.f) {  // drop weights <= thr x (this warp's running sum)
+      float t0 = l0, t1 = l1;
+#pragma unroll
+      for (int msk = 4; msk < 32; msk <<= 1) {
+        t0 += __shfl_xor_sync(0xffffffffu, t0, msk);
+        t1 += __shfl_xor_sync(0xffffffffu, t1, msk);
+      }
+      if (p00 <= a.sparse_thr * t0) p00 = 0.f;
+      if (p10 <= a.sparse_thr * t0) p10 = 0.f;
+      if (p01 <= a.sparse_thr * t1) p01 = 0.f;
+      if (p11 <= a.sparse_thr * t1) p11 = 0.f;
+    }
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+      for (int i = 0; i < NK; ++i) {
+        o[i][0] *= al0; o[i][1] *= al1; o[i][2] *= al0; o[i][3] *= al1;
+      }
+    }
+
+    // ---- P^T operand (hi + lo) from the accumulator layout
+    uint32_t x1h, x1l, x2h, x2l;
+    tc::split2<VT::BF>(p00, p01, x1h, x1l);
+    tc::split2<VT::BF>(p10, p11, x2h, x2l);
+    const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
+    const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+
+    // ---- O^T += V^T . P^T
+    if constexpr (VS == S_BF16) {
+      const int mi = lane >> 3, rr = lane & 7;
+      const uint8_t* base = vb + ((mi >> 1) * 8 + rr) * VT::VRS + (mi & 1) * 16;
+#pragma unroll
+      for (int i = 0; i < NK; ++i) {
+        uint32_t f[4];
+        tc::ldsm_x4_t(f, base + i * 32);
+        tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0h, b1h);
+        tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0l, b1l);
+      }
+    } else {  // FP8: tokens 2c, 2c+1, 2c+8, 2c+9; dims g*DPT .. g*DPT + DPT - 1
+      constexpr int DPT = HD / 8;
+      constexpr int W = DPT / 4;  // 32-bit words per token
+      uint32_t w[4][W];
+      const int toks[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint8_t* src = vb + toks[t] * VT::VRS + g * DPT;
+        if constexpr (W == 2) {
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          w[t][0] = v.x; w[t][1] = v.y;
+        } else {
+#pragma unroll
+          for (int q4 = 0; q4 < W / 4; ++q4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + q4 * 16);
+            w[t][4 * q4] = v.x; w[t][4 * q4 + 1] = v.y; w[t][4 * q4 + 2] = v.z; w[t][4 * q4 + 3] = v.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NK; ++i) {
+        const int wi = (2 * i) / 4;
+        const uint32_t sel = ((2 * i) % 4 == 0) ? 0x5140u : 0x7362u;
+        const uint32_t x01 = tc::prmt(w[0][wi], w[1][wi], sel);   // (t0,t1) @ dims 2i, 2i+1
+        const uint32_t x23 = tc::prmt(w[2][wi], w[3][wi], sel);   // (t2,t3)
+        const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
+        const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
+        tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
+        tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int msk = 4; msk < 32; msk <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
+  }
+  __syncthreads();  // every warp is done with its ring
+  float* mo = reinterpret_cast<float*>(rings);   // [4 warps][8 heads][HD]
+  float* ml = mo + 4 * 8 * HD;                   // [4 warps][8 heads][m, l]
+#pragma unroll
+  for (int i = 0; i < NK; ++i) {
+    const int da = v_row_dim<VS, HD>(i, g), db = v_row_dim<VS, HD>(i, g + 8);
+    mo[(warp * 8 + 2 * c) * HD + da] = o[i][0];
+    mo[(warp * 8 + 2 * c + 1) * HD + da] = o[i][1];
+    mo[(warp * 8 + 2 * c) * HD + db] = o[i][2];
+    mo[(warp * 8 + 2 * c + 1) * HD + db] = o[i][3];
+  }
+  if (g == 0) {
+    ml[(warp * 8 + 2 * c) * 2] = m0;
+    ml[(warp * 8 + 2 * c) * 2 + 1] = l0;
+    ml[(warp * 8 + 2 * c + 1) * 2] = m1;
+    ml[(warp * 8 + 2 * c + 1) * 2 + 1] = l1;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < a.rep * HD; idx += 128) {
+    const int r = idx / HD, d = idx - r * HD;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w2 = 0; w2 < 4; ++w2) M = fmaxf(M, ml[(w2 * 8 + r) * 2]);
+    float acc = 0.f, lsum = 0.f;
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int w2 = 0; w2 < 4; ++w2) {
+        const float f = exp2f(ml[(w2 * 8 + r) * 2] - M);
+        acc = fmaf(mo[(w2 * 8 + r) * HD + d], f, acc);
+        lsum = fmaf(ml[(w2 * 8 + r) * 2 + 1], f, lsum);
+      }
+    }
+    float* pp = part + r * pstride;
+    pp[4 + d] = acc * a.v_mult;
+    if (d == 0) {
+      pp[0] = M;
+      pp[1] = lsum;
+    }
+  }
+}
+
+template <int KS, int VS, int HD>
+cudaError_t launch_tc_inst(const DecodeArgs& a, cudaStream_t st) {
+  using C = TcCfg<KS, VS, HD>;
+  auto kern = decode_tc_kernel<KS, VS, HD>;
+  if (C::SMEM > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(a.nsplit, a.nkv, a.num_seqs);
+  kern<<<grid, 128, C::SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int KS, int VS>
+cudaError_t launch_tc_pair(int hd, const DecodeArgs& a, cudaStream_t st) {
+  switch (hd) {
+    case 64: return launch_tc_inst<KS, VS, 64>(a, st);
+    case 128: return launch_tc_inst<KS, VS, 128>(a, st);
+    case 256: return launch_tc_inst<KS, VS, 256>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq
