@@ -113,6 +113,15 @@ def algorithmic_decode_bytes(fmt, seq_lens, nkv, hd, bs, window=0):
     return int(att.sum()) * per_tok
 
 
+def decode_kernel_name(fmt):
+    """Name of the split-K kernel libkvq launches for this format (label only)."""
+    from quantized_paged_kv_reshape_gb300 import _abi as A
+    f = A.kvq_format_from_string(fmt)
+    sides = {A.kvq_side_format(f, 0), A.kvq_side_format(f, 1)}
+    tc = sides <= {0} or sides <= {1}
+    return "decode_tc_kernel" if tc else "decode_split_kernel"
+
+
 def write_bytes(fmt, ntok, nkv, hd, bs, in_bytes=2):
     from quantized_paged_kv_reshape_gb300 import ops
     out = sum(ops.block_bytes(fmt, side, bs, nkv, hd) // bs for side in (0, 1)) * ntok
@@ -299,7 +308,7 @@ def run_gpu(args):
                    "l2": f"inputs larger than L2 ({sum(dec_bytes.values()) / 1e6:.0f} MB of cache per step)",
                    "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
         "per_format": per_fmt,
-        "roofline": {"kernel": f"decode_split_kernel ({dom})", "bound": "hbm",
+        "roofline": {"kernel": f"{decode_kernel_name(dom)} ({dom}) + combine_kernel", "bound": "hbm",
                      "achieved": per_fmt[dom]["decode_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": round(per_fmt[dom]["decode_gbs"] / peak, 4),
                      "traffic": None, "peak_kind": peak_kind + " (hbm_gbs copy)",

@@ -76,6 +76,7 @@ typedef enum kvq_status {
 /* Device-side error bits written to *error_flag (never a fault). */
 #define KVQ_DEVERR_SLOT 1   /* write: slot >= num_blocks * block_size        */
 #define KVQ_DEVERR_BLOCK 2  /* decode: block table entry outside the pool    */
+#define KVQ_DEVERR_TIMEOUT 4 /* decode: a bounded wait for a page copy gave up */
 
 /* Combined cache formats, in the order of [ATLAS] enum KvCacheDtype.
  * kv_pair: the symmetric formats store the same side format in both pools;

@@ -264,11 +264,13 @@ decode_tc_kernel(const DecodeArgs a) {
                        : (lane < 16 ? (int64_t)b * a.k_bstride + ridx * KT::ROW
                                     : (int64_t)b * a.v_bstride + ridx * VT::ROW);
     __syncwarp();
-    constexpr int KC = KT::ROW / 16, VC = VT::ROW / 16;
+    constexpr int KC = KT::ROW / 16, VC = VT::ROW / 16;  // 16-byte chunks per row
+    constexpr int NQ = 16 * (KC + VC) / 32;                // copies per lane
+    static_assert((16 * KC) % 32 == 0 && (16 * VC) % 32 == 0, "whole copies per side");
 #pragma unroll
-    for (int q = lane; q < 16 * (KC + VC); q += 32) {
-      const bool isv = q >= 16 * KC;
-      const int q2 = isv ? q - 16 * KC : q;
+    for (int k = 0; k < NQ; ++k) {
+      const bool isv = k >= 16 * KC / 32;                   // compile-time per k
+      const int q2 = lane + 32 * (isv ? k - 16 * KC / 32 : k);
       const int row = isv ? q2 / VC : q2 / KC;
       const int ch = isv ? q2 % VC : q2 % KC;
       const int64_t off = offs[isv ? 16 + row : row];
@@ -302,6 +304,7 @@ decode_tc_kernel(const DecodeArgs a) {
 
     // ---- S^T = K . Q^T
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    float sacl[4] = {0.f, 0.f, 0.f, 0.f};   // second, independent MMA chain
     if constexpr (KS == S_BF16) {
       const int mi = lane >> 3, rr = lane & 7;
       const uint8_t* base = kb + ((mi & 1) * 8 + rr) * KT::KRS + (mi >> 1) * 16;
@@ -310,7 +313,7 @@ decode_tc_kernel(const DecodeArgs a) {
         uint32_t f[4];
         tc::ldsm_x4(f, base + j * 32);
         tc::mma<true>(sacc, f[0], f[1], f[2], f[3], qh[j][0], qh[j][1]);
-        tc::mma<true>(sacc, f[0], f[1], f[2], f[3], ql[j][0], ql[j][1]);
+        tc::mma<true>(sacl, f[0], f[1], f[2], f[3], ql[j][0], ql[j][1]);
       }
     } else {  // FP8: thread c converts 16-byte chunks 4jj + c of rows g and g+8
 #pragma unroll
@@ -325,10 +328,12 @@ decode_tc_kernel(const DecodeArgs a) {
           const uint32_t a0 = tc::e4m3x2_f16x2(wa[e] & 0xffffu), a4 = tc::e4m3x2_f16x2(wa[e] >> 16);
           const uint32_t a2 = tc::e4m3x2_f16x2(wb[e] & 0xffffu), a6 = tc::e4m3x2_f16x2(wb[e] >> 16);
           tc::mma<false>(sacc, a0, a2, a4, a6, qh[j][0], qh[j][1]);
-          tc::mma<false>(sacc, a0, a2, a4, a6, ql[j][0], ql[j][1]);
+          tc::mma<false>(sacl, a0, a2, a4, a6, ql[j][0], ql[j][1]);
         }
       }
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc[e] += sacl[e];
 
     // ---- online softmax; this thread holds rows (tokens) g, g+8, cols 2c, 2c+1
     const int slab_pos = tok0 + (warp + 4 * s) * 16;
