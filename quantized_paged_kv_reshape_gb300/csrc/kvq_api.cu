@@ -146,7 +146,10 @@ struct SplitPlan {
 
 // Flash-decoding split: enough CTAs of (split, kv head, sequence) to fill the
 // SMs several times, each split at least two 32-token tiles long.
-SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, int sms) {
+// ctas_per_sm: 3 for the tensor-core kernel (long splits amortize its
+// prologue and merge), 6 for the CUDA-core kernel (measured on GB300).
+SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, int sms,
+                     int ctas_per_sm) {
   const int tp = 32 / bs;
   int pages = max_blocks;
   if (window > 0) {
@@ -155,7 +158,7 @@ SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, 
   }
   if (pages < 1) pages = 1;
   const int64_t units = (int64_t)num_seqs * nkv;
-  const int64_t target = (int64_t)(sms > 0 ? sms : 148) * 6;
+  const int64_t target = (int64_t)(sms > 0 ? sms : 148) * ctas_per_sm;
   int64_t ns = units > 0 ? (target + units - 1) / units : 1;
   const int64_t max_ns = std::max<int64_t>(1, pages / (2 * tp));
   ns = std::min(std::max<int64_t>(ns, 1), max_ns);
@@ -164,6 +167,10 @@ SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, 
   if (pps > 512) pps = 512;  // the tensor-core kernel stages a split's block ids in smem
   const int nsplit = (pages + pps - 1) / pps;
   return {nsplit, pps};
+}
+
+int split_ctas_per_sm(kvq_format fmt) {
+  return decode_tc_supported(side_of(fmt, 0), side_of(fmt, 1)) ? 3 : 6;
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -343,7 +350,8 @@ size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t nq, int32_t nkv, int
   if (!fmt_ok(fmt) || num_seqs < 0 || nq < 1 || nkv < 1 || hd < 1 || bs < 1 || max_blocks < 1 ||
       window < 0 || (bs != 8 && bs != 16 && bs != 32))
     return 0;
-  const SplitPlan p = plan_split(num_seqs, nkv, bs, max_blocks, window, sm_count());
+  const SplitPlan p = plan_split(num_seqs, nkv, bs, max_blocks, window, sm_count(),
+                                 split_ctas_per_sm(fmt));
   return (size_t)num_seqs * nq * p.nsplit * (hd + 4) * sizeof(float);
 }
 
@@ -384,7 +392,7 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
       (vs == S_FP8 && !(v_scale > 0.f && std::isfinite(v_scale))))
     return fail(KVQ_ERR_ARG, "FP8 side needs a finite scale > 0");
   const int sms = sm_count();
-  const SplitPlan p = plan_split(num_seqs, nkv, bs, max_blocks, window, sms);
+  const SplitPlan p = plan_split(num_seqs, nkv, bs, max_blocks, window, sms, split_ctas_per_sm(fmt));
   const size_t need = (size_t)num_seqs * nq * p.nsplit * (hd + 4) * sizeof(float);
   if (workspace_bytes < need)
     return fail(KVQ_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);

@@ -198,34 +198,6 @@ decode_tc_kernel(const DecodeArgs a) {
     return;
   }
 
-  // ---- queries (rotated when K is stored rotated), rows >= rep are zero
-  for (int j = warp; j < 8; j += 4) {
-    float x[E];
-    if (j < a.rep) {
-      const int64_t qoff = (int64_t)seq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
-#pragma unroll
-      for (int i = 0; i < E; ++i)
-        x[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
-                        : reinterpret_cast<const float*>(a.q)[qoff + i];
-      if constexpr (side_rotated(KS)) fwht_warp<E>(x, lane, a.inv_sqrt_hd);
-    } else {
-#pragma unroll
-      for (int i = 0; i < E; ++i) x[i] = 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < E; ++i) q_s[j * HD + lane * E + i] = x[i];
-  }
-  __syncthreads();
-  uint32_t qh[NK][2], ql[NK][2];
-#pragma unroll
-  for (int j = 0; j < NK; ++j) {
-    int d[4];
-    k_slot_dims<KS, HD>(j, c, d);
-    const float* qr = q_s + g * HD;
-    tc::split2<KT::BF>(qr[d[0]], qr[d[1]], qh[j][0], ql[j][0]);
-    tc::split2<KT::BF>(qr[d[2]], qr[d[3]], qh[j][1], ql[j][1]);
-  }
-
   const int tok0 = p0 * bs;
   const int tok_end = min(p1 * bs, L);
   const int nslab = (tok_end - tok0 + 15) / 16;
@@ -255,6 +227,7 @@ decode_tc_kernel(const DecodeArgs a) {
   // lanes 16-31: V row), then 16-byte copies with consecutive lanes on
   // consecutive chunks of the same row.
   auto issue = [&](int s) {
+    __syncwarp();  // the previous issue's reads of offs are done
     uint8_t* sb = ring + (s % C::NST) * C::STAGE;
     const int t = lane & 15;
     const int pos = tok0 + (warp + 4 * s) * 16 + t;
@@ -285,6 +258,34 @@ decode_tc_kernel(const DecodeArgs a) {
   for (int s = 0; s < C::NST - 1; ++s) {
     if (s < my) issue(s);
     cp_async_commit();
+  }
+
+  // ---- queries (rotated when K is stored rotated), rows >= rep are zero
+  for (int j = warp; j < 8; j += 4) {
+    float x[E];
+    if (j < a.rep) {
+      const int64_t qoff = (int64_t)seq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        x[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
+                        : reinterpret_cast<const float*>(a.q)[qoff + i];
+      if constexpr (side_rotated(KS)) fwht_warp<E>(x, lane, a.inv_sqrt_hd);
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) x[i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) q_s[j * HD + lane * E + i] = x[i];
+  }
+  __syncthreads();  // q_s complete (copies of the first slabs are in flight)
+  uint32_t qh[NK][2], ql[NK][2];
+#pragma unroll
+  for (int j = 0; j < NK; ++j) {
+    int d[4];
+    k_slot_dims<KS, HD>(j, c, d);
+    const float* qr = q_s + g * HD;
+    tc::split2<KT::BF>(qr[d[0]], qr[d[1]], qh[j][0], ql[j][0]);
+    tc::split2<KT::BF>(qr[d[2]], qr[d[3]], qh[j][1], ql[j][1]);
   }
 
   float o[NK][4];
