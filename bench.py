@@ -114,12 +114,9 @@ def algorithmic_decode_bytes(fmt, seq_lens, nkv, hd, bs, window=0):
 
 
 def decode_kernel_name(fmt):
-    """Name of the split-K kernel libkvq launches for this format (label only)."""
-    from quantized_paged_kv_reshape_gb300 import _abi as A
-    f = A.kvq_format_from_string(fmt)
-    sides = {A.kvq_side_format(f, 0), A.kvq_side_format(f, 1)}
-    tc = sides <= {0} or sides <= {1}
-    return "decode_tc_kernel" if tc else "decode_split_kernel"
+    """Name of the split-K kernel libkvq launches for this format (label only):
+    every catalogue format runs on the tensor-core kernel."""
+    return "decode_tc_kernel"
 
 
 def write_bytes(fmt, ntok, nkv, hd, bs, in_bytes=2):

@@ -428,7 +428,7 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   a.part = (float*)workspace;
   a.err = error_flag;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = decode_tc_supported(ks, vs) ? launch_decode_tc(ks, vs, hd, a, st)
+  cudaError_t e = decode_tc_supported(ks, vs) ? launch_decode_tc(ks, vs, hd, a, cb, st)
                                                : launch_decode(ks, vs, hd, rmax, a, cb, st);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   CombineArgs c{};

@@ -110,17 +110,32 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 
 }  // namespace tc
 
-// Per-side layout of the staged rows of one slab (16 positions).
+// Per-side layout of the staged rows of one slab (16 positions).  Row
+// strides are chosen so that the fragment loads of one warp touch distinct
+// banks (see the access pattern of each side in decode_tc_kernel).
 template <int S, int HD>
 struct TcSide {
-  static constexpr bool BF = S == S_BF16;
-  static constexpr int ROW = SideGeom<S, HD>::ROW;
-  // K rows: ldmatrix wants 8 rows at distinct 16-byte bank groups (stride
-  // = 16 mod 128); FP8 K chunks want rows 2k, 2k+1 in opposite halves of
-  // the banks (stride = 64 mod 128).
-  static constexpr int KRS = BF ? ROW + 16 : (ROW % 128 == 0 ? ROW + 64 : ROW);
-  // V rows: ldmatrix.trans as above; FP8 V reads tokens 2c,2c+1,2c+8,2c+9.
-  static constexpr int VRS = BF ? ROW + 16 : (HD == 64 ? 80 : HD == 128 ? 144 : ROW + 16);
+  static constexpr bool BF = S == S_BF16;                  // bf16 MMA operands (else fp16)
+  static constexpr bool CB = side_codebook(S);              // codes through the pair LUT
+  static constexpr bool GS = side_scale_bytes(S) > 0;       // per-16 group scales
+  static constexpr int BITS = side_bits(S);
+  static constexpr int ROW = SideGeom<S, HD>::ROW;          // data bytes per row
+  static constexpr int SROW = SideGeom<S, HD>::SROW;        // scale bytes per row
+  static constexpr int CH = ROW % 16 == 0 ? 16 : 8;         // copy chunk of data rows
+  static constexpr int SCH = SROW == 0 ? 0 : (SROW >= 16 ? 16 : SROW);
+  static constexpr int KRS =
+      S == S_BF16 ? ROW + 16
+      : S == S_FP8 ? (ROW % 128 == 0 ? ROW + 64 : ROW)
+      : S == S_T8 || S == S_T4 ? ROW + 16
+      : S == S_T3 ? (HD == 256 ? ROW + 16 : ROW)
+      : /* T2 */ (HD == 64 ? ROW : ROW + 16);
+  static constexpr int VRS =
+      S == S_BF16 ? ROW + 16
+      : S == S_FP8 ? (HD == 64 ? 80 : HD == 128 ? 144 : ROW + 16)
+      : S == S_T8 || S == S_T4 ? ROW + 16
+      : S == S_T3 ? (HD == 256 ? ROW + 16 : ROW)
+      : /* T2 */ (HD == 64 ? ROW : ROW + 16);
+  static constexpr int LUT_BYTES = CB ? (1 << (2 * code_bits(S))) * 16 * 8 : 0;
 };
 
 template <int KS, int VS, int HD>
@@ -128,27 +143,41 @@ struct TcCfg {
   using K = TcSide<KS, HD>;
   using V = TcSide<VS, HD>;
   static constexpr int NK = HD / 16;
-  static constexpr int STAGE = 16 * (K::KRS + V::VRS);
-  static constexpr int NST = (4 * 4 * STAGE <= 110 * 1024) ? 4 : (4 * 3 * STAGE <= 110 * 1024) ? 3 : 2;
+  // stage: [K rows][K scale rows][V rows][V scale rows]
+  static constexpr int OFF_KS = 16 * K::KRS;
+  static constexpr int OFF_V = OFF_KS + 16 * K::SROW;
+  static constexpr int OFF_VS = OFF_V + 16 * V::VRS;
+  static constexpr int STAGE = (OFF_VS + 16 * V::SROW + 15) / 16 * 16;
+  static constexpr bool SHARE_LUT = K::CB && V::CB && code_bits(KS) == code_bits(VS);
+  static constexpr int LUTS = K::LUT_BYTES + (SHARE_LUT ? 0 : V::LUT_BYTES);
   static constexpr int MAXP = 512;                             // pages per split (host cap)
   static constexpr int OFF_BLK = 8 * HD * 4;                   // after q_s [8][HD] fp32
   static constexpr int OFF_OFFS = OFF_BLK + MAXP * 4;          // int32 block ids of the split
-  static constexpr int OFF_RING = OFF_OFFS + 4 * 32 * 8;       // per-warp row offsets
+  static constexpr int OFF_LUT = OFF_OFFS + 4 * 32 * 8;        // per-warp row offsets
+  static constexpr int OFF_RING = OFF_LUT + LUTS;
+  static constexpr int BUDGET = 112 * 1024 - OFF_RING;         // two CTAs per SM
+  static constexpr int NST0 = BUDGET / (4 * STAGE);
+  static constexpr int NST = NST0 > 6 ? 6 : (NST0 < 2 ? 2 : NST0);
   static constexpr int RING = 4 * NST * STAGE;
   static constexpr int MERGE = 4 * 8 * HD * 4 + 4 * 8 * 2 * 4;
   static constexpr int SMEM = OFF_RING + (RING > MERGE ? RING : MERGE);
 };
 
-// Dims carried by the B fragment of k-step j for thread c: b0b1 = (d, d+1),
-// b2b3 = (d+2, d+3) with d = kdim(j, c) (FP8: permuted), or
-// b0b1 = (d, d+1), b2b3 = (d+8, d+9) with d = 16j + 2c (BF16: natural).
+// Dims carried by the B fragment of k-step j for thread c: b0b1 = (d0, d1),
+// b2b3 = (d2, d3).  BF16: natural ldmatrix order.  FP8: K's reduction
+// dimension permuted so that thread c converts whole 16-byte chunks.
+// Group-scaled sides: k-step j is the scale group j, thread c takes its
+// dims 4c .. 4c+3.
 template <int S, int HD>
 __device__ __forceinline__ void k_slot_dims(int j, int c, int (&d)[4]) {
   if constexpr (S == S_BF16) {
     const int b = 16 * j + 2 * c;
     d[0] = b; d[1] = b + 1; d[2] = b + 8; d[3] = b + 9;
-  } else {
+  } else if constexpr (S == S_FP8) {
     const int b = 16 * (4 * (j / 4) + c) + 4 * (j % 4);
+    d[0] = b; d[1] = b + 1; d[2] = b + 2; d[3] = b + 3;
+  } else {
+    const int b = 16 * j + 4 * c;
     d[0] = b; d[1] = b + 1; d[2] = b + 2; d[3] = b + 3;
   }
 }
@@ -158,15 +187,46 @@ template <int S, int HD>
 __device__ __forceinline__ int v_row_dim(int i, int row) {
   if constexpr (S == S_BF16) {
     return 16 * i + row;
-  } else {
+  } else if constexpr (S == S_FP8) {
     constexpr int DPT = HD / 8;  // dims per thread group g
     return (row & 7) * DPT + 2 * i + (row >> 3);
+  } else {  // group-scaled: rows g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1
+    return 16 * i + 2 * (row & 7) + (row >> 3);
   }
+}
+
+// Group scale g of a staged scale row (E4M3 for Turbo2/3/4, BF16 for Turbo8).
+template <int S>
+__device__ __forceinline__ float tc_group_scale(const uint8_t* srow, int g) {
+  if constexpr (S == S_T8)
+    return bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(srow + 2 * g));
+  else
+    return e4m3_to_float(srow[g]);
+}
+
+// Code pair (dims 2k, 2k+1 of one token, low code = first dim) starting at
+// bit `bit` of a staged code row.
+template <int B>
+__device__ __forceinline__ uint32_t code_pair(const uint8_t* row, int bit) {
+  if constexpr (B == 4) {
+    return row[bit >> 3];
+  } else if constexpr (B == 2) {
+    return ((uint32_t)row[bit >> 3] >> (bit & 7)) & 15u;
+  } else {  // 3-bit codes: a 6-bit field that may straddle two bytes
+    const uint32_t w = (uint32_t)row[bit >> 3] | ((uint32_t)row[(bit >> 3) + 1] << 8);
+    return (w >> (bit & 7)) & 63u;
+  }
+}
+
+// Pair LUT entry: (hi(c0), hi(c1)) and (lo(c0), lo(c1)) as fp16x2, copy
+// lane & 15 so that a half-warp's 8-byte loads fall in distinct banks.
+__device__ __forceinline__ uint2 lut_pair(const uint2* lut, uint32_t pair, int lane) {
+  return lut[pair * 16 + (lane & 15)];
 }
 
 template <int KS, int VS, int HD>
 __global__ void __launch_bounds__(128)
-decode_tc_kernel(const DecodeArgs a) {
+decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   using C = TcCfg<KS, VS, HD>;
   using KT = typename C::K;
   using VT = typename C::V;
@@ -175,6 +235,8 @@ decode_tc_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   float* q_s = reinterpret_cast<float*>(smem);
   uint8_t* rings = smem + C::OFF_RING;
+  const uint2* lut_k = reinterpret_cast<const uint2*>(smem + C::OFF_LUT);
+  const uint2* lut_v = reinterpret_cast<const uint2*>(smem + C::OFF_LUT + (C::SHARE_LUT ? 0 : KT::LUT_BYTES));
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -215,6 +277,23 @@ decode_tc_kernel(const DecodeArgs a) {
     if (bad && a.err) atomicOr(a.err, 2);
     blk_s[i] = bad ? -1 : (int)b;
   }
+  // Pair LUTs of the codebook sides: entry p = (code of dim 2k) | (code of
+  // dim 2k+1) << b holds fp16 (hi, hi) and (lo, lo) with level = hi + lo.
+  auto fill_lut = [&](uint2* lut, const float* lv, int bits) {
+    const int n = 1 << bits;
+    for (int e = tid; e < n * n * 16; e += 128) {
+      const int pr = e >> 4;
+      const float c0 = lv[pr & (n - 1)], c1 = lv[pr >> bits];
+      uint32_t hi, lo2;
+      tc::split2<false>(c0, c1, hi, lo2);
+      lut[e] = make_uint2(hi, lo2);
+    }
+  };
+  if constexpr (KT::CB)
+    fill_lut(reinterpret_cast<uint2*>(smem + C::OFF_LUT), side_levels<KS>(cb), code_bits(KS));
+  if constexpr (VT::CB && !C::SHARE_LUT)
+    fill_lut(reinterpret_cast<uint2*>(smem + C::OFF_LUT + KT::LUT_BYTES), side_levels<VS>(cb),
+             code_bits(VS));
   __syncthreads();
 
   // Block id of position pos, or -1 if it is not attended / not valid.
@@ -224,33 +303,62 @@ decode_tc_kernel(const DecodeArgs a) {
   };
 
   // Row byte offsets of the slab (lanes 0-15: K row of position t = lane,
-  // lanes 16-31: V row), then 16-byte copies with consecutive lanes on
-  // consecutive chunks of the same row.
+  // lanes 16-31: V row), then copies with consecutive lanes on consecutive
+  // chunks: K data, K scales, V data, V scales.
   auto issue = [&](int s) {
     __syncwarp();  // the previous issue's reads of offs are done
     uint8_t* sb = ring + (s % C::NST) * C::STAGE;
     const int t = lane & 15;
-    const int pos = tok0 + (warp + 4 * s) * 16 + t;
-    const int b = pos_block(pos);
-    const int64_t ridx = (int64_t)(pos & (bs - 1)) * a.nkv + kvh;
-    offs[lane] = b < 0 ? -1
-                       : (lane < 16 ? (int64_t)b * a.k_bstride + ridx * KT::ROW
-                                    : (int64_t)b * a.v_bstride + ridx * VT::ROW);
+    const int slab_pos = tok0 + (warp + 4 * s) * 16;
+    const int b = pos_block(slab_pos + t);
+    // byte offset of the block holding the row (data and scale sections are
+    // added per copy)
+    offs[lane] = b < 0 ? -1 : (lane < 16 ? (int64_t)b * a.k_bstride : (int64_t)b * a.v_bstride);
     __syncwarp();
-    constexpr int KC = KT::ROW / 16, VC = VT::ROW / 16;  // 16-byte chunks per row
-    constexpr int NQ = 16 * (KC + VC) / 32;                // copies per lane
-    static_assert((16 * KC) % 32 == 0 && (16 * VC) % 32 == 0, "whole copies per side");
+    constexpr int NKD = 16 * KT::ROW / KT::CH;
+    constexpr int NKS = KT::SCH ? 16 * KT::SROW / KT::SCH : 0;
+    constexpr int NVD = 16 * VT::ROW / VT::CH;
+    constexpr int NVS = VT::SCH ? 16 * VT::SROW / VT::SCH : 0;
+    constexpr int TOT = NKD + NKS + NVD + NVS;
 #pragma unroll
-    for (int k = 0; k < NQ; ++k) {
-      const bool isv = k >= 16 * KC / 32;                   // compile-time per k
-      const int q2 = lane + 32 * (isv ? k - 16 * KC / 32 : k);
-      const int row = isv ? q2 / VC : q2 / KC;
-      const int ch = isv ? q2 % VC : q2 % KC;
-      const int64_t off = offs[isv ? 16 + row : row];
-      const bool ok = off >= 0;
-      const uint8_t* src = (isv ? a.v_cache : a.k_cache) + (ok ? off : 0) + ch * 16;
-      uint8_t* dst = sb + (isv ? 16 * KT::KRS + row * VT::VRS : row * KT::KRS) + ch * 16;
-      cp_async<16>(dst, src, ok);
+    for (int k = 0; k < (TOT + 31) / 32; ++k) {
+      const int q = lane + 32 * k;
+      if (q < TOT) {
+        int row, ch, region;
+        if (q < NKD) { region = 0; row = q / (KT::ROW / KT::CH); ch = q % (KT::ROW / KT::CH); }
+        else if (q < NKD + NKS) { region = 1; const int q2 = q - NKD; row = q2 / (KT::SROW / KT::SCH); ch = q2 % (KT::SROW / KT::SCH); }
+        else if (q < NKD + NKS + NVD) { region = 2; const int q2 = q - NKD - NKS; row = q2 / (VT::ROW / VT::CH); ch = q2 % (VT::ROW / VT::CH); }
+        else { region = 3; const int q2 = q - NKD - NKS - NVD; row = q2 / (VT::SROW / VT::SCH); ch = q2 % (VT::SROW / VT::SCH); }
+        const bool isv = region >= 2;
+        const int64_t boff = offs[isv ? 16 + row : row];
+        const bool ok = boff >= 0;
+        // row index inside the block of position slab_pos + row
+        const int64_t rr = (int64_t)((slab_pos + row) & (bs - 1)) * a.nkv + kvh;
+        const uint8_t* base = isv ? a.v_cache : a.k_cache;
+        const uint8_t* src;
+        uint8_t* dst;
+        if (region == 0) {
+          src = base + (ok ? boff + rr * KT::ROW : 0) + ch * KT::CH;
+          dst = sb + row * KT::KRS + ch * KT::CH;
+          cp_async<KT::CH>(dst, src, ok);
+        } else if (region == 1) {
+          if constexpr (NKS > 0) {
+            src = base + (ok ? boff + a.k_dsec + rr * KT::SROW : 0) + ch * KT::SCH;
+            dst = sb + C::OFF_KS + row * KT::SROW + ch * KT::SCH;
+            cp_async<KT::SCH ? KT::SCH : 4>(dst, src, ok);
+          }
+        } else if (region == 2) {
+          src = base + (ok ? boff + rr * VT::ROW : 0) + ch * VT::CH;
+          dst = sb + C::OFF_V + row * VT::VRS + ch * VT::CH;
+          cp_async<VT::CH>(dst, src, ok);
+        } else {
+          if constexpr (NVS > 0) {
+            src = base + (ok ? boff + a.v_dsec + rr * VT::SROW : 0) + ch * VT::SCH;
+            dst = sb + C::OFF_VS + row * VT::SROW + ch * VT::SCH;
+            cp_async<VT::SCH ? VT::SCH : 4>(dst, src, ok);
+          }
+        }
+      }
     }
   };
 
@@ -301,7 +409,7 @@ decode_tc_kernel(const DecodeArgs a) {
     cp_async_commit();
     const uint8_t* sb = ring + (s % C::NST) * C::STAGE;
     const uint8_t* kb = sb;
-    const uint8_t* vb = sb + 16 * KT::KRS;
+    const uint8_t* vb = sb + C::OFF_V;
 
     // ---- S^T = K . Q^T
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -316,7 +424,7 @@ decode_tc_kernel(const DecodeArgs a) {
         tc::mma<true>(sacc, f[0], f[1], f[2], f[3], qh[j][0], qh[j][1]);
         tc::mma<true>(sacl, f[0], f[1], f[2], f[3], ql[j][0], ql[j][1]);
       }
-    } else {  // FP8: thread c converts 16-byte chunks 4jj + c of rows g and g+8
+    } else if constexpr (KS == S_FP8) {  // thread c converts 16-byte chunks 4jj + c of rows g, g+8
 #pragma unroll
       for (int jj = 0; jj < NK / 4; ++jj) {
         const uint4 ra = *reinterpret_cast<const uint4*>(kb + g * KT::KRS + (4 * jj + c) * 16);
@@ -331,6 +439,38 @@ decode_tc_kernel(const DecodeArgs a) {
           tc::mma<false>(sacc, a0, a2, a4, a6, qh[j][0], qh[j][1]);
           tc::mma<false>(sacl, a0, a2, a4, a6, ql[j][0], ql[j][1]);
         }
+      }
+    } else {  // group-scaled sides: k-step j is scale group j
+      const uint8_t* ra = kb + g * KT::KRS;
+      const uint8_t* rb = kb + (g + 8) * KT::KRS;
+      const uint8_t* sa = kb + C::OFF_KS + g * KT::SROW;
+      const uint8_t* sbr = kb + C::OFF_KS + (g + 8) * KT::SROW;
+#pragma unroll
+      for (int j = 0; j < NK; ++j) {
+        float cg[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (KS == S_T8) {
+          const uint32_t wa = *reinterpret_cast<const uint32_t*>(ra + 16 * j + 4 * c);
+          const uint32_t wb = *reinterpret_cast<const uint32_t*>(rb + 16 * j + 4 * c);
+          const uint32_t a0 = tc::e4m3x2_f16x2(wa & 0xffffu), a4 = tc::e4m3x2_f16x2(wa >> 16);
+          const uint32_t a2 = tc::e4m3x2_f16x2(wb & 0xffffu), a6 = tc::e4m3x2_f16x2(wb >> 16);
+          tc::mma<false>(cg, a0, a2, a4, a6, qh[j][0], qh[j][1]);
+          tc::mma<false>(cg, a0, a2, a4, a6, ql[j][0], ql[j][1]);
+        } else {
+          constexpr int B = code_bits(KS);
+          const int bit = B * (16 * j + 4 * c);
+          const uint2 xa0 = lut_pair(lut_k, code_pair<B>(ra, bit), lane);
+          const uint2 xa1 = lut_pair(lut_k, code_pair<B>(ra, bit + 2 * B), lane);
+          const uint2 xb0 = lut_pair(lut_k, code_pair<B>(rb, bit), lane);
+          const uint2 xb1 = lut_pair(lut_k, code_pair<B>(rb, bit + 2 * B), lane);
+          tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, qh[j][0], qh[j][1]);
+          tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
+          tc::mma<false>(cg, xa0.y, xb0.y, xa1.y, xb1.y, qh[j][0], qh[j][1]);
+        }
+        const float ga = tc_group_scale<KS>(sa, j), gb = tc_group_scale<KS>(sbr, j);
+        sacc[0] = fmaf(cg[0], ga, sacc[0]);
+        sacc[1] = fmaf(cg[1], ga, sacc[1]);
+        sacc[2] = fmaf(cg[2], gb, sacc[2]);
+        sacc[3] = fmaf(cg[3], gb, sacc[3]);
       }
     }
 #pragma unroll
@@ -385,53 +525,101 @@ decode_tc_kernel(const DecodeArgs a) {
       }
     }
 
-    // ---- P^T operand (hi + lo) from the accumulator layout
-    uint32_t x1h, x1l, x2h, x2l;
-    tc::split2<VT::BF>(p00, p01, x1h, x1l);
-    tc::split2<VT::BF>(p10, p11, x2h, x2l);
-    const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
-    const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
-
     // ---- O^T += V^T . P^T
-    if constexpr (VS == S_BF16) {
-      const int mi = lane >> 3, rr = lane & 7;
-      const uint8_t* base = vb + ((mi >> 1) * 8 + rr) * VT::VRS + (mi & 1) * 16;
+    if constexpr (!VT::GS) {
+      // P^T operand (hi + lo) from the accumulator layout
+      uint32_t x1h, x1l, x2h, x2l;
+      tc::split2<VT::BF>(p00, p01, x1h, x1l);
+      tc::split2<VT::BF>(p10, p11, x2h, x2l);
+      const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
+      const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+      if constexpr (VS == S_BF16) {
+        const int mi = lane >> 3, rr = lane & 7;
+        const uint8_t* base = vb + ((mi >> 1) * 8 + rr) * VT::VRS + (mi & 1) * 16;
 #pragma unroll
-      for (int i = 0; i < NK; ++i) {
-        uint32_t f[4];
-        tc::ldsm_x4_t(f, base + i * 32);
-        tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0h, b1h);
-        tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0l, b1l);
-      }
-    } else {  // FP8: tokens 2c, 2c+1, 2c+8, 2c+9; dims g*DPT .. g*DPT + DPT - 1
-      constexpr int DPT = HD / 8;
-      constexpr int W = DPT / 4;  // 32-bit words per token
-      uint32_t w[4][W];
-      const int toks[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+        for (int i = 0; i < NK; ++i) {
+          uint32_t f[4];
+          tc::ldsm_x4_t(f, base + i * 32);
+          tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0h, b1h);
+          tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0l, b1l);
+        }
+      } else {  // FP8: tokens 2c, 2c+1, 2c+8, 2c+9; dims g*DPT .. g*DPT + DPT - 1
+        constexpr int DPT = HD / 8;
+        constexpr int W = DPT / 4;  // 32-bit words per token
+        uint32_t w[4][W];
+        const int toks[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint8_t* src = vb + toks[t] * VT::VRS + g * DPT;
-        if constexpr (W == 2) {
-          const uint2 v = *reinterpret_cast<const uint2*>(src);
-          w[t][0] = v.x; w[t][1] = v.y;
-        } else {
+        for (int t = 0; t < 4; ++t) {
+          const uint8_t* src = vb + toks[t] * VT::VRS + g * DPT;
+          if constexpr (W == 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(src);
+            w[t][0] = v.x; w[t][1] = v.y;
+          } else {
 #pragma unroll
-          for (int q4 = 0; q4 < W / 4; ++q4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(src + q4 * 16);
-            w[t][4 * q4] = v.x; w[t][4 * q4 + 1] = v.y; w[t][4 * q4 + 2] = v.z; w[t][4 * q4 + 3] = v.w;
+            for (int q4 = 0; q4 < W / 4; ++q4) {
+              const uint4 v = *reinterpret_cast<const uint4*>(src + q4 * 16);
+              w[t][4 * q4] = v.x; w[t][4 * q4 + 1] = v.y; w[t][4 * q4 + 2] = v.z; w[t][4 * q4 + 3] = v.w;
+            }
           }
         }
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+          const int wi = (2 * i) / 4;
+          const uint32_t sel = ((2 * i) % 4 == 0) ? 0x5140u : 0x7362u;
+          const uint32_t x01 = tc::prmt(w[0][wi], w[1][wi], sel);   // (t0,t1) @ dims 2i, 2i+1
+          const uint32_t x23 = tc::prmt(w[2][wi], w[3][wi], sel);   // (t2,t3)
+          const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
+          const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
+          tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
+          tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
+        }
       }
+    } else {
+      // Group-scaled V: m-tile i is scale group i; P is scaled per token by
+      // its group scale before the split.  Rows g, g+8 of m-tile i are dims
+      // 16i + 2g, 16i + 2g + 1; k-slots are tokens 2c, 2c+1, 2c+8, 2c+9.
+      const uint8_t* vsa = vb + (C::OFF_VS - C::OFF_V) + g * VT::SROW;
+      const uint8_t* vsb = vb + (C::OFF_VS - C::OFF_V) + (g + 8) * VT::SROW;
+      const uint8_t* r0 = vb + (2 * c) * VT::VRS;
+      const uint8_t* r1 = vb + (2 * c + 1) * VT::VRS;
+      const uint8_t* r2 = vb + (2 * c + 8) * VT::VRS;
+      const uint8_t* r3 = vb + (2 * c + 9) * VT::VRS;
 #pragma unroll
       for (int i = 0; i < NK; ++i) {
-        const int wi = (2 * i) / 4;
-        const uint32_t sel = ((2 * i) % 4 == 0) ? 0x5140u : 0x7362u;
-        const uint32_t x01 = tc::prmt(w[0][wi], w[1][wi], sel);   // (t0,t1) @ dims 2i, 2i+1
-        const uint32_t x23 = tc::prmt(w[2][wi], w[3][wi], sel);   // (t2,t3)
-        const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
-        const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
-        tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
-        tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
+        const float ga = tc_group_scale<VS>(vsa, i), gb = tc_group_scale<VS>(vsb, i);
+        uint32_t x1h, x1l, x2h, x2l;
+        tc::split2<false>(p00 * ga, p01 * ga, x1h, x1l);
+        tc::split2<false>(p10 * gb, p11 * gb, x2h, x2l);
+        const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
+        const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+        if constexpr (VS == S_T8) {
+          const int off = 16 * i + 2 * g;
+          const uint32_t u0 = *reinterpret_cast<const uint16_t*>(r0 + off);
+          const uint32_t u1 = *reinterpret_cast<const uint16_t*>(r1 + off);
+          const uint32_t u2 = *reinterpret_cast<const uint16_t*>(r2 + off);
+          const uint32_t u3 = *reinterpret_cast<const uint16_t*>(r3 + off);
+          const uint32_t x01 = tc::prmt(u0, u1, 0x5140u);   // (t0,t1) @ dims 2g, 2g+1
+          const uint32_t x23 = tc::prmt(u2, u3, 0x5140u);
+          const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
+          const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
+          tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
+          tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
+        } else {
+          constexpr int B = code_bits(VS);
+          const int bit = B * (16 * i + 2 * g);
+          const uint2 e0 = lut_pair(lut_v, code_pair<B>(r0, bit), lane);
+          const uint2 e1 = lut_pair(lut_v, code_pair<B>(r1, bit), lane);
+          const uint2 e2 = lut_pair(lut_v, code_pair<B>(r2, bit), lane);
+          const uint2 e3 = lut_pair(lut_v, code_pair<B>(r3, bit), lane);
+          // regroup (dim, dim+1) pairs of one token into (token, token) pairs
+          const uint32_t h0 = tc::prmt(e0.x, e1.x, 0x5410u), h2 = tc::prmt(e0.x, e1.x, 0x7632u);
+          const uint32_t h4 = tc::prmt(e2.x, e3.x, 0x5410u), h6 = tc::prmt(e2.x, e3.x, 0x7632u);
+          const uint32_t l0_ = tc::prmt(e0.y, e1.y, 0x5410u), l2_ = tc::prmt(e0.y, e1.y, 0x7632u);
+          const uint32_t l4_ = tc::prmt(e2.y, e3.y, 0x5410u), l6_ = tc::prmt(e2.y, e3.y, 0x7632u);
+          tc::mma<false>(o[i], h0, h2, h4, h6, b0h, b1h);
+          tc::mma<false>(o[i], h0, h2, h4, h6, b0l, b1l);
+          tc::mma<false>(o[i], l0_, l2_, l4_, l6_, b0h, b1h);
+        }
       }
     }
   }
@@ -484,24 +672,25 @@ decode_tc_kernel(const DecodeArgs a) {
 }
 
 template <int KS, int VS, int HD>
-cudaError_t launch_tc_inst(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_tc_inst(const DecodeArgs& a, const Codebooks& cb, cudaStream_t st) {
   using C = TcCfg<KS, VS, HD>;
+  static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
   auto kern = decode_tc_kernel<KS, VS, HD>;
   if (C::SMEM > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(a.nsplit, a.nkv, a.num_seqs);
-  kern<<<grid, 128, C::SMEM, st>>>(a);
+  kern<<<grid, 128, C::SMEM, st>>>(a, cb);
   return cudaGetLastError();
 }
 
 template <int KS, int VS>
-cudaError_t launch_tc_pair(int hd, const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_tc_pair(int hd, const DecodeArgs& a, const Codebooks& cb, cudaStream_t st) {
   switch (hd) {
-    case 64: return launch_tc_inst<KS, VS, 64>(a, st);
-    case 128: return launch_tc_inst<KS, VS, 128>(a, st);
-    case 256: return launch_tc_inst<KS, VS, 256>(a, st);
+    case 64: return launch_tc_inst<KS, VS, 64>(a, cb, st);
+    case 128: return launch_tc_inst<KS, VS, 128>(a, cb, st);
+    case 256: return launch_tc_inst<KS, VS, 256>(a, cb, st);
     default: return cudaErrorInvalidValue;
   }
 }

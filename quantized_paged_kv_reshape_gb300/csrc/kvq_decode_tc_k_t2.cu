@@ -1,0 +1,17 @@
+// Tensor-core decode instances whose K side is T2 (one translation unit
+// per K side so the instances compile in parallel).  V sides: the
+// catalogue's pairs with this K side ("spark_runtime/kv_cache.rs",
+// KvCacheDtype::kv_pair).
+#include "kvq_decode_mma.cuh"
+
+namespace kvq {
+
+cudaError_t launch_tc_k_t2(int v_side, int hd, const DecodeArgs& a, const Codebooks& cb,
+                              cudaStream_t st) {
+  switch (v_side) {
+    case S_T2: return launch_tc_pair<S_T2, S_T2>(hd, a, cb, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

@@ -88,9 +88,16 @@ size_t smem_k_t2(int v_side, int hd, int rmax);
 size_t smem_k_t8(int v_side, int hd, int rmax);
 
 
-// Tensor-core decode (kvq_decode_tc.cu) for the pairs it supports.
+// Tensor-core decode (kvq_decode_tc_k_*.cu) for the pairs it supports.
 bool decode_tc_supported(int k_side, int v_side);
-cudaError_t launch_decode_tc(int k_side, int v_side, int hd, const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_tc(int k_side, int v_side, int hd, const DecodeArgs& a,
+                             const Codebooks& cb, cudaStream_t st);
+cudaError_t launch_tc_k_bf16(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tc_k_fp8(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tc_k_t4(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tc_k_t3(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tc_k_t2(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tc_k_t8(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 
 // Shared memory bytes the decode instance needs (0 if no instance).
 size_t decode_smem_bytes(int k_side, int v_side, int head_dim, int rmax);
