@@ -23,7 +23,7 @@
 // fragments permuted accordingly.
 //
 // Each warp owns a private cp.async ring of slabs (no CTA barrier inside the
-// loop); the 4 warps of a CTA take slabs w, w+4, ... of the split and are
+// loop); the NW warps of a CTA take slabs w, w+NW, ... of the split and are
 // merged through shared memory at the end.  Positions outside [lo, L), past
 // the split or with a bad block id are zero-filled and masked to -inf.
 #pragma once
@@ -97,6 +97,18 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   const float2 h = unpack2<BF>(hi);
   lo = pack2<BF>(x0 - h.x, x1 - h.y);
 }
+// x rounded to 7 significant bits (round to nearest even on the fp32 bits);
+// exact in fp16 for the magnitudes used here.
+__device__ __forceinline__ float round_sig7(float x) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t r = (b + 0xffffu + ((b >> 17) & 1u)) & ~0x1ffffu;
+  return __uint_as_float(r);
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t lo16) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"((unsigned short)lo16));
@@ -138,8 +150,18 @@ struct TcSide {
   static constexpr int LUT_BYTES = CB ? (1 << (2 * code_bits(S))) * 16 * 8 : 0;
 };
 
+// Warps per CTA: 8 when a side goes through the codebook LUT (one LUT per
+// CTA serves more warps, and the longer dependent chains need more warps in
+// flight) and head_dim <= 128 (the 128-register budget of 16 warps per SM
+// holds the accumulators), else 4.
+template <int KS, int VS, int HD>
+struct TcWarps {
+  static constexpr int NW = ((side_codebook(KS) || side_codebook(VS)) && HD <= 128) ? 8 : 4;
+};
+
 template <int KS, int VS, int HD>
 struct TcCfg {
+  static constexpr int NW = TcWarps<KS, VS, HD>::NW;
   using K = TcSide<KS, HD>;
   using V = TcSide<VS, HD>;
   static constexpr int NK = HD / 16;
@@ -153,13 +175,13 @@ struct TcCfg {
   static constexpr int MAXP = 512;                             // pages per split (host cap)
   static constexpr int OFF_BLK = 8 * HD * 4;                   // after q_s [8][HD] fp32
   static constexpr int OFF_OFFS = OFF_BLK + MAXP * 4;          // int32 block ids of the split
-  static constexpr int OFF_LUT = OFF_OFFS + 4 * 32 * 8;        // per-warp row offsets
+  static constexpr int OFF_LUT = OFF_OFFS + NW * 32 * 8;       // per-warp row offsets
   static constexpr int OFF_RING = OFF_LUT + LUTS;
   static constexpr int BUDGET = 112 * 1024 - OFF_RING;         // two CTAs per SM
-  static constexpr int NST0 = BUDGET / (4 * STAGE);
+  static constexpr int NST0 = BUDGET / (NW * STAGE);
   static constexpr int NST = NST0 > 6 ? 6 : (NST0 < 2 ? 2 : NST0);
-  static constexpr int RING = 4 * NST * STAGE;
-  static constexpr int MERGE = 4 * 8 * HD * 4 + 4 * 8 * 2 * 4;
+  static constexpr int RING = NW * NST * STAGE;
+  static constexpr int MERGE = NW * 8 * HD * 4 + NW * 8 * 2 * 4;
   static constexpr int SMEM = OFF_RING + (RING > MERGE ? RING : MERGE);
 };
 
@@ -225,9 +247,11 @@ __device__ __forceinline__ uint2 lut_pair(const uint2* lut, uint32_t pair, int l
 }
 
 template <int KS, int VS, int HD>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(32 * TcWarps<KS, VS, HD>::NW, 2)
 decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   using C = TcCfg<KS, VS, HD>;
+  constexpr int NW = C::NW;
+  constexpr int NT = 32 * NW;
   using KT = typename C::K;
   using VT = typename C::V;
   constexpr int NK = C::NK;
@@ -255,7 +279,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   const size_t pstride = (size_t)a.nsplit * (HD + 4);
   float* part = a.part + ((size_t)(seq * a.nq + kvh * a.rep) * a.nsplit + split) * (HD + 4);
   if (p0 >= p1) {
-    for (int j = warp; j < a.rep; j += 4)
+    for (int j = warp; j < a.rep; j += NW)
       for (int i = lane; i < HD + 4; i += 32) part[j * pstride + i] = (i == 0) ? -CUDART_INF_F : 0.f;
     return;
   }
@@ -263,7 +287,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   const int tok0 = p0 * bs;
   const int tok_end = min(p1 * bs, L);
   const int nslab = (tok_end - tok0 + 15) / 16;
-  const int my = nslab > warp ? (nslab - 1 - warp) / 4 + 1 : 0;
+  const int my = nslab > warp ? (nslab - 1 - warp) / NW + 1 : 0;
   const int64_t tab = (int64_t)seq * a.max_blocks;
   uint8_t* ring = rings + warp * C::NST * C::STAGE;
   int* blk_s = reinterpret_cast<int*>(smem + C::OFF_BLK);
@@ -271,22 +295,25 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   const int lbs = 31 - __clz(bs);  // block_size is a power of two
 
   // Block ids of the split's pages, staged once (-1 = outside the pool).
-  for (int i = tid; i < p1 - p0; i += 128) {
+  for (int i = tid; i < p1 - p0; i += NT) {
     const int64_t b = a.block_tables[tab + p0 + i];
     const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
     if (bad && a.err) atomicOr(a.err, 2);
     blk_s[i] = bad ? -1 : (int)b;
   }
   // Pair LUTs of the codebook sides: entry p = (code of dim 2k) | (code of
-  // dim 2k+1) << b holds fp16 (hi, hi) and (lo, lo) with level = hi + lo.
+  // dim 2k+1) << b holds fp16 (hi, hi) and (lo, lo) where hi and lo carry 7
+  // significant bits each and level = hi + lo to ~2^-16 relative.  With 7
+  // bits, hi and lo times an E4M3 group scale (4 significant bits) are exact
+  // in fp16, which lets the V operand absorb its group scale.
   auto fill_lut = [&](uint2* lut, const float* lv, int bits) {
     const int n = 1 << bits;
-    for (int e = tid; e < n * n * 16; e += 128) {
+    for (int e = tid; e < n * n * 16; e += NT) {
       const int pr = e >> 4;
       const float c0 = lv[pr & (n - 1)], c1 = lv[pr >> bits];
-      uint32_t hi, lo2;
-      tc::split2<false>(c0, c1, hi, lo2);
-      lut[e] = make_uint2(hi, lo2);
+      const float h0 = tc::round_sig7(c0), h1 = tc::round_sig7(c1);
+      const float l0 = tc::round_sig7(c0 - h0), l1 = tc::round_sig7(c1 - h1);
+      lut[e] = make_uint2(tc::pack2<false>(h0, h1), tc::pack2<false>(l0, l1));
     }
   };
   if constexpr (KT::CB)
@@ -309,7 +336,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     __syncwarp();  // the previous issue's reads of offs are done
     uint8_t* sb = ring + (s % C::NST) * C::STAGE;
     const int t = lane & 15;
-    const int slab_pos = tok0 + (warp + 4 * s) * 16;
+    const int slab_pos = tok0 + (warp + NW * s) * 16;
     const int b = pos_block(slab_pos + t);
     // byte offset of the block holding the row (data and scale sections are
     // added per copy)
@@ -369,7 +396,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   }
 
   // ---- queries (rotated when K is stored rotated), rows >= rep are zero
-  for (int j = warp; j < 8; j += 4) {
+  for (int j = warp; j < 8; j += NW) {
     float x[E];
     if (j < a.rep) {
       const int64_t qoff = (int64_t)seq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
@@ -445,6 +472,12 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       const uint8_t* rb = kb + (g + 8) * KT::KRS;
       const uint8_t* sa = kb + C::OFF_KS + g * KT::SROW;
       const uint8_t* sbr = kb + C::OFF_KS + (g + 8) * KT::SROW;
+      float gsa[NK], gsb[NK];   // group scales of rows g and g+8
+#pragma unroll
+      for (int j = 0; j < NK; ++j) {
+        gsa[j] = tc_group_scale<KS>(sa, j);
+        gsb[j] = tc_group_scale<KS>(sbr, j);
+      }
 #pragma unroll
       for (int j = 0; j < NK; ++j) {
         float cg[4] = {0.f, 0.f, 0.f, 0.f};
@@ -458,26 +491,40 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
         } else {
           constexpr int B = code_bits(KS);
           const int bit = B * (16 * j + 4 * c);
-          const uint2 xa0 = lut_pair(lut_k, code_pair<B>(ra, bit), lane);
-          const uint2 xa1 = lut_pair(lut_k, code_pair<B>(ra, bit + 2 * B), lane);
-          const uint2 xb0 = lut_pair(lut_k, code_pair<B>(rb, bit), lane);
-          const uint2 xb1 = lut_pair(lut_k, code_pair<B>(rb, bit + 2 * B), lane);
+          uint32_t pa0, pa1, pb0, pb1;   // code pairs (dims 4c,4c+1) and (4c+2,4c+3)
+          if constexpr (B == 4) {
+            const uint32_t ua = *reinterpret_cast<const uint16_t*>(ra + (bit >> 3));
+            const uint32_t ub = *reinterpret_cast<const uint16_t*>(rb + (bit >> 3));
+            pa0 = ua & 0xffu; pa1 = ua >> 8; pb0 = ub & 0xffu; pb1 = ub >> 8;
+          } else if constexpr (B == 2) {
+            const uint32_t ua = ra[bit >> 3], ub = rb[bit >> 3];
+            pa0 = ua & 15u; pa1 = ua >> 4; pb0 = ub & 15u; pb1 = ub >> 4;
+          } else {
+            const int sh = bit & 7;
+            const uint32_t ua = ((uint32_t)ra[bit >> 3] | ((uint32_t)ra[(bit >> 3) + 1] << 8)) >> sh;
+            const uint32_t ub = ((uint32_t)rb[bit >> 3] | ((uint32_t)rb[(bit >> 3) + 1] << 8)) >> sh;
+            pa0 = ua & 63u; pa1 = (ua >> 6) & 63u; pb0 = ub & 63u; pb1 = (ub >> 6) & 63u;
+          }
+          const uint2 xa0 = lut_pair(lut_k, pa0, lane);
+          const uint2 xa1 = lut_pair(lut_k, pa1, lane);
+          const uint2 xb0 = lut_pair(lut_k, pb0, lane);
+          const uint2 xb1 = lut_pair(lut_k, pb1, lane);
           tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, qh[j][0], qh[j][1]);
           tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
           tc::mma<false>(cg, xa0.y, xb0.y, xa1.y, xb1.y, qh[j][0], qh[j][1]);
         }
-        const float ga = tc_group_scale<KS>(sa, j), gb = tc_group_scale<KS>(sbr, j);
-        sacc[0] = fmaf(cg[0], ga, sacc[0]);
-        sacc[1] = fmaf(cg[1], ga, sacc[1]);
-        sacc[2] = fmaf(cg[2], gb, sacc[2]);
-        sacc[3] = fmaf(cg[3], gb, sacc[3]);
+        float* acc = (j & 1) ? sacl : sacc;   // two independent accumulators
+        acc[0] = fmaf(cg[0], gsa[j], acc[0]);
+        acc[1] = fmaf(cg[1], gsa[j], acc[1]);
+        acc[2] = fmaf(cg[2], gsb[j], acc[2]);
+        acc[3] = fmaf(cg[3], gsb[j], acc[3]);
       }
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) sacc[e] += sacl[e];
 
     // ---- online softmax; this thread holds rows (tokens) g, g+8, cols 2c, 2c+1
-    const int slab_pos = tok0 + (warp + 4 * s) * 16;
+    const int slab_pos = tok0 + (warp + NW * s) * 16;
     const bool va = pos_block(slab_pos + g) >= 0;
     const bool vb_ = pos_block(slab_pos + g + 8) >= 0;
     const float s00 = va ? sacc[0] * scale : -CUDART_INF_F;
@@ -574,10 +621,61 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
           tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
         }
       }
+    } else if constexpr (VT::CB) {
+      // Codebook V: m-tile i is scale group i.  The operand is (level hi,
+      // level lo) x group scale of its token, exact in fp16 (7-bit level
+      // parts, 4-bit scale significand), so P is split once per slab.  Rows
+      // g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1; k-slots are
+      // tokens 2c, 2c+1, 2c+8, 2c+9.
+      uint32_t x1h, x1l, x2h, x2l;
+      tc::split2<false>(p00, p01, x1h, x1l);
+      tc::split2<false>(p10, p11, x2h, x2l);
+      const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
+      const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+      const uint8_t* r0 = vb + (2 * c) * VT::VRS;
+      const uint8_t* r1 = vb + (2 * c + 1) * VT::VRS;
+      const uint8_t* r2 = vb + (2 * c + 8) * VT::VRS;
+      const uint8_t* r3 = vb + (2 * c + 9) * VT::VRS;
+      const uint8_t* vsc = vb + (C::OFF_VS - C::OFF_V);
+      constexpr int SW = (VT::SROW + 3) / 4;   // 32-bit words of a scale row
+      uint32_t s0[SW], s1[SW], s2[SW], s3[SW];
+#pragma unroll
+      for (int q4 = 0; q4 < SW; ++q4) {
+        s0[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c) * VT::SROW + 4 * q4);
+        s1[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 1) * VT::SROW + 4 * q4);
+        s2[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 8) * VT::SROW + 4 * q4);
+        s3[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 9) * VT::SROW + 4 * q4);
+      }
+#pragma unroll
+      for (int i = 0; i < NK; ++i) {
+        constexpr int B = code_bits(VS);
+        const int bit = B * (16 * i + 2 * g);
+        const uint2 e0 = lut_pair(lut_v, code_pair<B>(r0, bit), lane);
+        const uint2 e1 = lut_pair(lut_v, code_pair<B>(r1, bit), lane);
+        const uint2 e2 = lut_pair(lut_v, code_pair<B>(r2, bit), lane);
+        const uint2 e3 = lut_pair(lut_v, code_pair<B>(r3, bit), lane);
+        // group scales of the four tokens as fp16 pairs (t0,t1), (t2,t3)
+        const uint32_t bsel = (uint32_t)(i & 3) | ((uint32_t)(4 + (i & 3)) << 4);
+        const uint32_t sc01 = tc::e4m3x2_f16x2(tc::prmt(s0[i >> 2], s1[i >> 2], bsel));
+        const uint32_t sc23 = tc::e4m3x2_f16x2(tc::prmt(s2[i >> 2], s3[i >> 2], bsel));
+        // regroup (dim, dim+1) pairs of one token into (token, token) pairs
+        const uint32_t h0 = tc::hmul2(tc::prmt(e0.x, e1.x, 0x5410u), sc01);
+        const uint32_t h2 = tc::hmul2(tc::prmt(e0.x, e1.x, 0x7632u), sc01);
+        const uint32_t h4 = tc::hmul2(tc::prmt(e2.x, e3.x, 0x5410u), sc23);
+        const uint32_t h6 = tc::hmul2(tc::prmt(e2.x, e3.x, 0x7632u), sc23);
+        const uint32_t l0_ = tc::hmul2(tc::prmt(e0.y, e1.y, 0x5410u), sc01);
+        const uint32_t l2_ = tc::hmul2(tc::prmt(e0.y, e1.y, 0x7632u), sc01);
+        const uint32_t l4_ = tc::hmul2(tc::prmt(e2.y, e3.y, 0x5410u), sc23);
+        const uint32_t l6_ = tc::hmul2(tc::prmt(e2.y, e3.y, 0x7632u), sc23);
+        tc::mma<false>(o[i], h0, h2, h4, h6, b0h, b1h);
+        tc::mma<false>(o[i], h0, h2, h4, h6, b0l, b1l);
+        tc::mma<false>(o[i], l0_, l2_, l4_, l6_, b0h, b1h);
+      }
     } else {
-      // Group-scaled V: m-tile i is scale group i; P is scaled per token by
-      // its group scale before the split.  Rows g, g+8 of m-tile i are dims
-      // 16i + 2g, 16i + 2g + 1; k-slots are tokens 2c, 2c+1, 2c+8, 2c+9.
+      // Turbo8 V: m-tile i is scale group i; P is scaled per token by its
+      // BF16 group scale before the split (E4M3 x BF16 is not exact in
+      // fp16).  Rows g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1;
+      // k-slots are tokens 2c, 2c+1, 2c+8, 2c+9.
       const uint8_t* vsa = vb + (C::OFF_VS - C::OFF_V) + g * VT::SROW;
       const uint8_t* vsb = vb + (C::OFF_VS - C::OFF_V) + (g + 8) * VT::SROW;
       const uint8_t* r0 = vb + (2 * c) * VT::VRS;
@@ -592,7 +690,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
         tc::split2<false>(p10 * gb, p11 * gb, x2h, x2l);
         const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
         const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
-        if constexpr (VS == S_T8) {
+        {
           const int off = 16 * i + 2 * g;
           const uint32_t u0 = *reinterpret_cast<const uint16_t*>(r0 + off);
           const uint32_t u1 = *reinterpret_cast<const uint16_t*>(r1 + off);
@@ -604,21 +702,6 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
           const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
           tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
           tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
-        } else {
-          constexpr int B = code_bits(VS);
-          const int bit = B * (16 * i + 2 * g);
-          const uint2 e0 = lut_pair(lut_v, code_pair<B>(r0, bit), lane);
-          const uint2 e1 = lut_pair(lut_v, code_pair<B>(r1, bit), lane);
-          const uint2 e2 = lut_pair(lut_v, code_pair<B>(r2, bit), lane);
-          const uint2 e3 = lut_pair(lut_v, code_pair<B>(r3, bit), lane);
-          // regroup (dim, dim+1) pairs of one token into (token, token) pairs
-          const uint32_t h0 = tc::prmt(e0.x, e1.x, 0x5410u), h2 = tc::prmt(e0.x, e1.x, 0x7632u);
-          const uint32_t h4 = tc::prmt(e2.x, e3.x, 0x5410u), h6 = tc::prmt(e2.x, e3.x, 0x7632u);
-          const uint32_t l0_ = tc::prmt(e0.y, e1.y, 0x5410u), l2_ = tc::prmt(e0.y, e1.y, 0x7632u);
-          const uint32_t l4_ = tc::prmt(e2.y, e3.y, 0x5410u), l6_ = tc::prmt(e2.y, e3.y, 0x7632u);
-          tc::mma<false>(o[i], h0, h2, h4, h6, b0h, b1h);
-          tc::mma<false>(o[i], h0, h2, h4, h6, b0l, b1l);
-          tc::mma<false>(o[i], l0_, l2_, l4_, l6_, b0h, b1h);
         }
       }
     }
@@ -631,8 +714,8 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
   }
   __syncthreads();  // every warp is done with its ring
-  float* mo = reinterpret_cast<float*>(rings);   // [4 warps][8 heads][HD]
-  float* ml = mo + 4 * 8 * HD;                   // [4 warps][8 heads][m, l]
+  float* mo = reinterpret_cast<float*>(rings);   // [NW warps][8 heads][HD]
+  float* ml = mo + NW * 8 * HD;                  // [NW warps][8 heads][m, l]
 #pragma unroll
   for (int i = 0; i < NK; ++i) {
     const int da = v_row_dim<VS, HD>(i, g), db = v_row_dim<VS, HD>(i, g + 8);
@@ -648,15 +731,15 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     ml[(warp * 8 + 2 * c + 1) * 2 + 1] = l1;
   }
   __syncthreads();
-  for (int idx = tid; idx < a.rep * HD; idx += 128) {
+  for (int idx = tid; idx < a.rep * HD; idx += NT) {
     const int r = idx / HD, d = idx - r * HD;
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int w2 = 0; w2 < 4; ++w2) M = fmaxf(M, ml[(w2 * 8 + r) * 2]);
+    for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, ml[(w2 * 8 + r) * 2]);
     float acc = 0.f, lsum = 0.f;
     if (M != -CUDART_INF_F) {
 #pragma unroll
-      for (int w2 = 0; w2 < 4; ++w2) {
+      for (int w2 = 0; w2 < NW; ++w2) {
         const float f = exp2f(ml[(w2 * 8 + r) * 2] - M);
         acc = fmaf(mo[(w2 * 8 + r) * HD + d], f, acc);
         lsum = fmaf(ml[(w2 * 8 + r) * 2 + 1], f, lsum);
@@ -681,7 +764,7 @@ cudaError_t launch_tc_inst(const DecodeArgs& a, const Codebooks& cb, cudaStream_
     if (e != cudaSuccess) return e;
   }
   dim3 grid(a.nsplit, a.nkv, a.num_seqs);
-  kern<<<grid, 128, C::SMEM, st>>>(a, cb);
+  kern<<<grid, 32 * C::NW, C::SMEM, st>>>(a, cb);
   return cudaGetLastError();
 }
 
