@@ -30,6 +30,8 @@
 
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "kvq_decode.cuh"
 
 namespace kvq {
@@ -150,13 +152,21 @@ struct TcSide {
   static constexpr int LUT_BYTES = CB ? (1 << (2 * code_bits(S))) * 16 * 8 : 0;
 };
 
-// Warps per CTA: 8 when a side goes through the codebook LUT (one LUT per
-// CTA serves more warps, and the longer dependent chains need more warps in
-// flight) and head_dim <= 128 (the 128-register budget of 16 warps per SM
-// holds the accumulators), else 4.
+// Warps per CTA (measured on GB300): 8 for head_dim <= 128 except BF16 K
+// (16 warps per SM hide the dependent MMA / LUT chains; one codebook LUT per
+// CTA serves more warps), 4 for BF16 K (its 8.5 KB slabs need the shared
+// memory for pipeline depth) and for head_dim 256 (accumulators exceed the
+// 128-register budget of 16 warps per SM).
+#ifndef KVQ_TC_NW_CB
+#define KVQ_TC_NW_CB 8
+#endif
+#ifndef KVQ_TC_NW_RAW
+#define KVQ_TC_NW_RAW 8
+#endif
 template <int KS, int VS, int HD>
 struct TcWarps {
-  static constexpr int NW = ((side_codebook(KS) || side_codebook(VS)) && HD <= 128) ? 8 : 4;
+  static constexpr bool CBS = side_codebook(KS) || side_codebook(VS);
+  static constexpr int NW = HD > 128 ? 4 : CBS ? KVQ_TC_NW_CB : (KS == S_BF16 ? 4 : KVQ_TC_NW_RAW);
 };
 
 template <int KS, int VS, int HD>
@@ -175,7 +185,7 @@ struct TcCfg {
   static constexpr int MAXP = 512;                             // pages per split (host cap)
   static constexpr int OFF_BLK = 8 * HD * 4;                   // after q_s [8][HD] fp32
   static constexpr int OFF_OFFS = OFF_BLK + MAXP * 4;          // int32 block ids of the split
-  static constexpr int OFF_LUT = OFF_OFFS + NW * 32 * 8;       // per-warp row offsets
+  static constexpr int OFF_LUT = OFF_OFFS + NW * 64 * 8;       // per-warp row offsets
   static constexpr int OFF_RING = OFF_LUT + LUTS;
   static constexpr int BUDGET = 112 * 1024 - OFF_RING;         // two CTAs per SM
   static constexpr int NST0 = BUDGET / (NW * STAGE);
@@ -215,6 +225,13 @@ __device__ __forceinline__ int v_row_dim(int i, int row) {
   } else {  // group-scaled: rows g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1
     return 16 * i + 2 * (row & 7) + (row >> 3);
   }
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  __half2_raw h;
+  h.x = (unsigned short)(v & 0xffffu);
+  h.y = (unsigned short)(v >> 16);
+  return __half22float2(__half2(h));
 }
 
 // Group scale g of a staged scale row (E4M3 for Turbo2/3/4, BF16 for Turbo8).
@@ -291,7 +308,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   const int64_t tab = (int64_t)seq * a.max_blocks;
   uint8_t* ring = rings + warp * C::NST * C::STAGE;
   int* blk_s = reinterpret_cast<int*>(smem + C::OFF_BLK);
-  int64_t* offs = reinterpret_cast<int64_t*>(smem + C::OFF_OFFS) + warp * 32;
+  int64_t* offs = reinterpret_cast<int64_t*>(smem + C::OFF_OFFS) + warp * 64;
   const int lbs = 31 - __clz(bs);  // block_size is a power of two
 
   // Block ids of the split's pages, staged once (-1 = outside the pool).
@@ -329,64 +346,52 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     return blk_s[(pos >> lbs) - p0];
   };
 
-  // Row byte offsets of the slab (lanes 0-15: K row of position t = lane,
-  // lanes 16-31: V row), then copies with consecutive lanes on consecutive
-  // chunks: K data, K scales, V data, V scales.
+  // Per slab, lanes 0-15 compute the source byte offsets of the K data and
+  // K scale rows of position t = lane, lanes 16-31 those of the V rows (-1
+  // for positions not attended); then four copy loops move the rows in
+  // chunks, consecutive lanes on consecutive chunks of a row.
+  auto copy_rows = [&](uint8_t* dst, int dst_stride, const uint8_t* base, const int64_t* tbl,
+                       auto rowbytes_c, auto chunk_c) {
+    constexpr int RB = decltype(rowbytes_c)::value, CHB = decltype(chunk_c)::value;
+    constexpr int NC = RB / CHB, TOT = 16 * NC;
+#pragma unroll
+    for (int k = 0; k < (TOT + 31) / 32; ++k) {
+      const int q = lane + 32 * k;
+      if (TOT % 32 == 0 || q < TOT) {
+        const int row = q / NC, ch = q - row * NC;
+        const int64_t off = tbl[row];
+        const bool ok = off >= 0;
+        cp_async<CHB>(dst + row * dst_stride + ch * CHB, base + (ok ? off : 0) + ch * CHB, ok);
+      }
+    }
+  };
   auto issue = [&](int s) {
     __syncwarp();  // the previous issue's reads of offs are done
     uint8_t* sb = ring + (s % C::NST) * C::STAGE;
     const int t = lane & 15;
     const int slab_pos = tok0 + (warp + NW * s) * 16;
     const int b = pos_block(slab_pos + t);
-    // byte offset of the block holding the row (data and scale sections are
-    // added per copy)
-    offs[lane] = b < 0 ? -1 : (lane < 16 ? (int64_t)b * a.k_bstride : (int64_t)b * a.v_bstride);
-    __syncwarp();
-    constexpr int NKD = 16 * KT::ROW / KT::CH;
-    constexpr int NKS = KT::SCH ? 16 * KT::SROW / KT::SCH : 0;
-    constexpr int NVD = 16 * VT::ROW / VT::CH;
-    constexpr int NVS = VT::SCH ? 16 * VT::SROW / VT::SCH : 0;
-    constexpr int TOT = NKD + NKS + NVD + NVS;
-#pragma unroll
-    for (int k = 0; k < (TOT + 31) / 32; ++k) {
-      const int q = lane + 32 * k;
-      if (q < TOT) {
-        int row, ch, region;
-        if (q < NKD) { region = 0; row = q / (KT::ROW / KT::CH); ch = q % (KT::ROW / KT::CH); }
-        else if (q < NKD + NKS) { region = 1; const int q2 = q - NKD; row = q2 / (KT::SROW / KT::SCH); ch = q2 % (KT::SROW / KT::SCH); }
-        else if (q < NKD + NKS + NVD) { region = 2; const int q2 = q - NKD - NKS; row = q2 / (VT::ROW / VT::CH); ch = q2 % (VT::ROW / VT::CH); }
-        else { region = 3; const int q2 = q - NKD - NKS - NVD; row = q2 / (VT::SROW / VT::SCH); ch = q2 % (VT::SROW / VT::SCH); }
-        const bool isv = region >= 2;
-        const int64_t boff = offs[isv ? 16 + row : row];
-        const bool ok = boff >= 0;
-        // row index inside the block of position slab_pos + row
-        const int64_t rr = (int64_t)((slab_pos + row) & (bs - 1)) * a.nkv + kvh;
-        const uint8_t* base = isv ? a.v_cache : a.k_cache;
-        const uint8_t* src;
-        uint8_t* dst;
-        if (region == 0) {
-          src = base + (ok ? boff + rr * KT::ROW : 0) + ch * KT::CH;
-          dst = sb + row * KT::KRS + ch * KT::CH;
-          cp_async<KT::CH>(dst, src, ok);
-        } else if (region == 1) {
-          if constexpr (NKS > 0) {
-            src = base + (ok ? boff + a.k_dsec + rr * KT::SROW : 0) + ch * KT::SCH;
-            dst = sb + C::OFF_KS + row * KT::SROW + ch * KT::SCH;
-            cp_async<KT::SCH ? KT::SCH : 4>(dst, src, ok);
-          }
-        } else if (region == 2) {
-          src = base + (ok ? boff + rr * VT::ROW : 0) + ch * VT::CH;
-          dst = sb + C::OFF_V + row * VT::VRS + ch * VT::CH;
-          cp_async<VT::CH>(dst, src, ok);
-        } else {
-          if constexpr (NVS > 0) {
-            src = base + (ok ? boff + a.v_dsec + rr * VT::SROW : 0) + ch * VT::SCH;
-            dst = sb + C::OFF_VS + row * VT::SROW + ch * VT::SCH;
-            cp_async<VT::SCH ? VT::SCH : 4>(dst, src, ok);
-          }
-        }
-      }
+    const int64_t rr = (int64_t)((slab_pos + t) & (bs - 1)) * a.nkv + kvh;   // row in block
+    if (lane < 16) {
+      const int64_t bo = (int64_t)b * a.k_bstride;
+      offs[t] = b < 0 ? -1 : bo + rr * KT::ROW;
+      offs[32 + t] = b < 0 ? -1 : bo + a.k_dsec + rr * KT::SROW;
+    } else {
+      const int64_t bo = (int64_t)b * a.v_bstride;
+      offs[16 + t] = b < 0 ? -1 : bo + rr * VT::ROW;
+      offs[48 + t] = b < 0 ? -1 : bo + a.v_dsec + rr * VT::SROW;
     }
+    __syncwarp();
+    copy_rows(sb, KT::KRS, a.k_cache, offs, std::integral_constant<int, KT::ROW>{},
+              std::integral_constant<int, KT::CH>{});
+    if constexpr (KT::SROW > 0)
+      copy_rows(sb + C::OFF_KS, KT::SROW, a.k_cache, offs + 32,
+                std::integral_constant<int, KT::SROW>{}, std::integral_constant<int, KT::SCH>{});
+    copy_rows(sb + C::OFF_V, VT::VRS, a.v_cache, offs + 16, std::integral_constant<int, VT::ROW>{},
+              std::integral_constant<int, VT::CH>{});
+    if constexpr (VT::SROW > 0)
+      copy_rows(sb + C::OFF_VS, VT::SROW, a.v_cache, offs + 48,
+                std::integral_constant<int, VT::SROW>{}, std::integral_constant<int, VT::SCH>{});
   };
 
 #pragma unroll
@@ -472,12 +477,6 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       const uint8_t* rb = kb + (g + 8) * KT::KRS;
       const uint8_t* sa = kb + C::OFF_KS + g * KT::SROW;
       const uint8_t* sbr = kb + C::OFF_KS + (g + 8) * KT::SROW;
-      float gsa[NK], gsb[NK];   // group scales of rows g and g+8
-#pragma unroll
-      for (int j = 0; j < NK; ++j) {
-        gsa[j] = tc_group_scale<KS>(sa, j);
-        gsb[j] = tc_group_scale<KS>(sbr, j);
-      }
 #pragma unroll
       for (int j = 0; j < NK; ++j) {
         float cg[4] = {0.f, 0.f, 0.f, 0.f};
@@ -513,11 +512,23 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
           tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
           tc::mma<false>(cg, xa0.y, xb0.y, xa1.y, xb1.y, qh[j][0], qh[j][1]);
         }
+        float ga, gb;   // group-j scales of rows g and g+8
+        if constexpr (KS == S_T8) {
+          ga = tc_group_scale<KS>(sa, j);
+          gb = tc_group_scale<KS>(sbr, j);
+        } else {
+          const float2 gs = unpack_f16x2(tc::e4m3x2_f16x2(
+              tc::prmt(*reinterpret_cast<const uint32_t*>(sa + (j & ~3)),
+                       *reinterpret_cast<const uint32_t*>(sbr + (j & ~3)),
+                       (uint32_t)(j & 3) | ((uint32_t)(4 + (j & 3)) << 4))));
+          ga = gs.x;
+          gb = gs.y;
+        }
         float* acc = (j & 1) ? sacl : sacc;   // two independent accumulators
-        acc[0] = fmaf(cg[0], gsa[j], acc[0]);
-        acc[1] = fmaf(cg[1], gsa[j], acc[1]);
-        acc[2] = fmaf(cg[2], gsb[j], acc[2]);
-        acc[3] = fmaf(cg[3], gsb[j], acc[3]);
+        acc[0] = fmaf(cg[0], ga, acc[0]);
+        acc[1] = fmaf(cg[1], ga, acc[1]);
+        acc[2] = fmaf(cg[2], gb, acc[2]);
+        acc[3] = fmaf(cg[3], gb, acc[3]);
       }
     }
 #pragma unroll
