@@ -175,17 +175,22 @@ struct TcCfg {
   using K = TcSide<KS, HD>;
   using V = TcSide<VS, HD>;
   static constexpr int NK = HD / 16;
-  // stage: [K rows][K scale rows][V rows][V scale rows]
-  static constexpr int OFF_KS = 16 * K::KRS;
-  static constexpr int OFF_V = OFF_KS + 16 * K::SROW;
-  static constexpr int OFF_VS = OFF_V + 16 * V::VRS;
-  static constexpr int STAGE = (OFF_VS + 16 * V::SROW + 15) / 16 * 16;
+  // token positions per warp iteration: one 16-row MMA tile (32-row
+  // iterations measured slower on GB300: fewer pipeline stages fit and the
+  // register budget spills)
+  static constexpr int SLAB = 16;
+  static constexpr int NH = SLAB / 16;
+  // stage: [K rows][K scale rows][V rows][V scale rows], SLAB rows each
+  static constexpr int OFF_KS = SLAB * K::KRS;
+  static constexpr int OFF_V = OFF_KS + SLAB * K::SROW;
+  static constexpr int OFF_VS = OFF_V + SLAB * V::VRS;
+  static constexpr int STAGE = (OFF_VS + SLAB * V::SROW + 15) / 16 * 16;
   static constexpr bool SHARE_LUT = K::CB && V::CB && code_bits(KS) == code_bits(VS);
   static constexpr int LUTS = K::LUT_BYTES + (SHARE_LUT ? 0 : V::LUT_BYTES);
   static constexpr int MAXP = 512;                             // pages per split (host cap)
   static constexpr int OFF_BLK = 8 * HD * 4;                   // after q_s [8][HD] fp32
   static constexpr int OFF_OFFS = OFF_BLK + MAXP * 4;          // int32 block ids of the split
-  static constexpr int OFF_LUT = OFF_OFFS + NW * 64 * 8;       // per-warp row offsets
+  static constexpr int OFF_LUT = OFF_OFFS + NW * 128 * 8;      // per-warp row offsets
   static constexpr int OFF_RING = OFF_LUT + LUTS;
   static constexpr int BUDGET = 112 * 1024 - OFF_RING;         // two CTAs per SM
   static constexpr int NST0 = BUDGET / (NW * STAGE);
@@ -303,12 +308,13 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
 
   const int tok0 = p0 * bs;
   const int tok_end = min(p1 * bs, L);
-  const int nslab = (tok_end - tok0 + 15) / 16;
+  constexpr int SLAB = C::SLAB;
+  const int nslab = (tok_end - tok0 + SLAB - 1) / SLAB;
   const int my = nslab > warp ? (nslab - 1 - warp) / NW + 1 : 0;
   const int64_t tab = (int64_t)seq * a.max_blocks;
   uint8_t* ring = rings + warp * C::NST * C::STAGE;
   int* blk_s = reinterpret_cast<int*>(smem + C::OFF_BLK);
-  int64_t* offs = reinterpret_cast<int64_t*>(smem + C::OFF_OFFS) + warp * 64;
+  int64_t* offs = reinterpret_cast<int64_t*>(smem + C::OFF_OFFS) + warp * 128;
   const int lbs = 31 - __clz(bs);  // block_size is a power of two
 
   // Block ids of the split's pages, staged once (-1 = outside the pool).
@@ -353,7 +359,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   auto copy_rows = [&](uint8_t* dst, int dst_stride, const uint8_t* base, const int64_t* tbl,
                        auto rowbytes_c, auto chunk_c) {
     constexpr int RB = decltype(rowbytes_c)::value, CHB = decltype(chunk_c)::value;
-    constexpr int NC = RB / CHB, TOT = 16 * NC;
+    constexpr int NC = RB / CHB, TOT = SLAB * NC;
 #pragma unroll
     for (int k = 0; k < (TOT + 31) / 32; ++k) {
       const int q = lane + 32 * k;
@@ -368,29 +374,26 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   auto issue = [&](int s) {
     __syncwarp();  // the previous issue's reads of offs are done
     uint8_t* sb = ring + (s % C::NST) * C::STAGE;
-    const int t = lane & 15;
-    const int slab_pos = tok0 + (warp + NW * s) * 16;
-    const int b = pos_block(slab_pos + t);
-    const int64_t rr = (int64_t)((slab_pos + t) & (bs - 1)) * a.nkv + kvh;   // row in block
-    if (lane < 16) {
-      const int64_t bo = (int64_t)b * a.k_bstride;
-      offs[t] = b < 0 ? -1 : bo + rr * KT::ROW;
-      offs[32 + t] = b < 0 ? -1 : bo + a.k_dsec + rr * KT::SROW;
-    } else {
-      const int64_t bo = (int64_t)b * a.v_bstride;
-      offs[16 + t] = b < 0 ? -1 : bo + rr * VT::ROW;
-      offs[48 + t] = b < 0 ? -1 : bo + a.v_dsec + rr * VT::SROW;
+    const int slab_pos = tok0 + (warp + NW * s) * SLAB;
+    const int b = pos_block(slab_pos + lane);
+    const int64_t rr = (int64_t)((slab_pos + lane) & (bs - 1)) * a.nkv + kvh;   // row in block
+    const int64_t bk = (int64_t)b * a.k_bstride, bv = (int64_t)b * a.v_bstride;
+    if (lane < SLAB) {
+      offs[lane] = b < 0 ? -1 : bk + rr * KT::ROW;
+      offs[32 + lane] = b < 0 ? -1 : bv + rr * VT::ROW;
+      offs[64 + lane] = b < 0 ? -1 : bk + a.k_dsec + rr * KT::SROW;
+      offs[96 + lane] = b < 0 ? -1 : bv + a.v_dsec + rr * VT::SROW;
     }
     __syncwarp();
     copy_rows(sb, KT::KRS, a.k_cache, offs, std::integral_constant<int, KT::ROW>{},
               std::integral_constant<int, KT::CH>{});
     if constexpr (KT::SROW > 0)
-      copy_rows(sb + C::OFF_KS, KT::SROW, a.k_cache, offs + 32,
+      copy_rows(sb + C::OFF_KS, KT::SROW, a.k_cache, offs + 64,
                 std::integral_constant<int, KT::SROW>{}, std::integral_constant<int, KT::SCH>{});
-    copy_rows(sb + C::OFF_V, VT::VRS, a.v_cache, offs + 16, std::integral_constant<int, VT::ROW>{},
+    copy_rows(sb + C::OFF_V, VT::VRS, a.v_cache, offs + 32, std::integral_constant<int, VT::ROW>{},
               std::integral_constant<int, VT::CH>{});
     if constexpr (VT::SROW > 0)
-      copy_rows(sb + C::OFF_VS, VT::SROW, a.v_cache, offs + 48,
+      copy_rows(sb + C::OFF_VS, VT::SROW, a.v_cache, offs + 96,
                 std::integral_constant<int, VT::SROW>{}, std::integral_constant<int, VT::SCH>{});
   };
 
@@ -434,134 +437,294 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
   const float scale = a.score_scale;
 
+  // S^T of the 16 positions whose K rows start at kbh (scale rows at ksbh).
+  auto scores16 = [&](const uint8_t* kbh, const uint8_t* ksbh, float (&sout)[4]) {
+    // ---- S^T = K . Q^T for the 16 rows at kbh (K rows) / ksbh (K scale rows)
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      float sacl[4] = {0.f, 0.f, 0.f, 0.f};   // second, independent MMA chain
+      if constexpr (KS == S_BF16) {
+        const int mi = lane >> 3, rr = lane & 7;
+        const uint8_t* base = kbh + ((mi & 1) * 8 + rr) * KT::KRS + (mi >> 1) * 16;
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+          uint32_t f[4];
+          tc::ldsm_x4(f, base + j * 32);
+          tc::mma<true>(sacc, f[0], f[1], f[2], f[3], qh[j][0], qh[j][1]);
+          tc::mma<true>(sacl, f[0], f[1], f[2], f[3], ql[j][0], ql[j][1]);
+        }
+      } else if constexpr (KS == S_FP8) {  // thread c converts 16-byte chunks 4jj + c of rows g, g+8
+#pragma unroll
+        for (int jj = 0; jj < NK / 4; ++jj) {
+          const uint4 ra = *reinterpret_cast<const uint4*>(kbh + g * KT::KRS + (4 * jj + c) * 16);
+          const uint4 rb = *reinterpret_cast<const uint4*>(kbh + (g + 8) * KT::KRS + (4 * jj + c) * 16);
+          const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
+          const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * jj + e;
+            const uint32_t a0 = tc::e4m3x2_f16x2(wa[e] & 0xffffu), a4 = tc::e4m3x2_f16x2(wa[e] >> 16);
+            const uint32_t a2 = tc::e4m3x2_f16x2(wb[e] & 0xffffu), a6 = tc::e4m3x2_f16x2(wb[e] >> 16);
+            tc::mma<false>(sacc, a0, a2, a4, a6, qh[j][0], qh[j][1]);
+            tc::mma<false>(sacl, a0, a2, a4, a6, ql[j][0], ql[j][1]);
+          }
+        }
+      } else {  // group-scaled sides: k-step j is scale group j
+        const uint8_t* ra = kbh + g * KT::KRS;
+        const uint8_t* rb = kbh + (g + 8) * KT::KRS;
+        const uint8_t* sa = ksbh + g * KT::SROW;
+        const uint8_t* sbr = ksbh + (g + 8) * KT::SROW;
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+          float cg[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (KS == S_T8) {
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(ra + 16 * j + 4 * c);
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(rb + 16 * j + 4 * c);
+            const uint32_t a0 = tc::e4m3x2_f16x2(wa & 0xffffu), a4 = tc::e4m3x2_f16x2(wa >> 16);
+            const uint32_t a2 = tc::e4m3x2_f16x2(wb & 0xffffu), a6 = tc::e4m3x2_f16x2(wb >> 16);
+            tc::mma<false>(cg, a0, a2, a4, a6, qh[j][0], qh[j][1]);
+            tc::mma<false>(cg, a0, a2, a4, a6, ql[j][0], ql[j][1]);
+          } else {
+            constexpr int B = code_bits(KS);
+            const int bit = B * (16 * j + 4 * c);
+            uint32_t pa0, pa1, pb0, pb1;   // code pairs (dims 4c,4c+1) and (4c+2,4c+3)
+            if constexpr (B == 4) {
+              const uint32_t ua = *reinterpret_cast<const uint16_t*>(ra + (bit >> 3));
+              const uint32_t ub = *reinterpret_cast<const uint16_t*>(rb + (bit >> 3));
+              pa0 = ua & 0xffu; pa1 = ua >> 8; pb0 = ub & 0xffu; pb1 = ub >> 8;
+            } else if constexpr (B == 2) {
+              const uint32_t ua = ra[bit >> 3], ub = rb[bit >> 3];
+              pa0 = ua & 15u; pa1 = ua >> 4; pb0 = ub & 15u; pb1 = ub >> 4;
+            } else {
+              const int sh = bit & 7;
+              const uint32_t ua = ((uint32_t)ra[bit >> 3] | ((uint32_t)ra[(bit >> 3) + 1] << 8)) >> sh;
+              const uint32_t ub = ((uint32_t)rb[bit >> 3] | ((uint32_t)rb[(bit >> 3) + 1] << 8)) >> sh;
+              pa0 = ua & 63u; pa1 = (ua >> 6) & 63u; pb0 = ub & 63u; pb1 = (ub >> 6) & 63u;
+            }
+            const uint2 xa0 = lut_pair(lut_k, pa0, lane);
+            const uint2 xa1 = lut_pair(lut_k, pa1, lane);
+            const uint2 xb0 = lut_pair(lut_k, pb0, lane);
+            const uint2 xb1 = lut_pair(lut_k, pb1, lane);
+            tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, qh[j][0], qh[j][1]);
+            tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
+            tc::mma<false>(cg, xa0.y, xb0.y, xa1.y, xb1.y, qh[j][0], qh[j][1]);
+          }
+          float ga, gb;   // group-j scales of rows g and g+8
+          if constexpr (KS == S_T8) {
+            ga = tc_group_scale<KS>(sa, j);
+            gb = tc_group_scale<KS>(sbr, j);
+          } else {
+            const float2 gs = unpack_f16x2(tc::e4m3x2_f16x2(
+                tc::prmt(*reinterpret_cast<const uint32_t*>(sa + (j & ~3)),
+                         *reinterpret_cast<const uint32_t*>(sbr + (j & ~3)),
+                         (uint32_t)(j & 3) | ((uint32_t)(4 + (j & 3)) << 4))));
+            ga = gs.x;
+            gb = gs.y;
+          }
+          float* acc = (j & 1) ? sacl : sacc;   // two independent accumulators
+          acc[0] = fmaf(cg[0], ga, acc[0]);
+          acc[1] = fmaf(cg[1], ga, acc[1]);
+          acc[2] = fmaf(cg[2], gb, acc[2]);
+          acc[3] = fmaf(cg[3], gb, acc[3]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[e] += sacl[e];
+
+      sout[0] = sacc[0]; sout[1] = sacc[1]; sout[2] = sacc[2]; sout[3] = sacc[3];
+  };
+  // O^T += V^T . P^T for the 16 positions whose V rows start at vbh (scale
+  // rows at vsbh); p00, p01 (row g) and p10, p11 (row g+8) are this
+  // thread's weights in the accumulator layout.
+  auto pv16 = [&](const uint8_t* vbh, const uint8_t* vsbh, float p00, float p01, float p10,
+                  float p11) {
+    // ---- O^T += V^T . P^T
+      if constexpr (!VT::GS) {
+        // P^T operand (hi + lo) from the accumulator layout
+        uint32_t x1h, x1l, x2h, x2l;
+        tc::split2<VT::BF>(p00, p01, x1h, x1l);
+        tc::split2<VT::BF>(p10, p11, x2h, x2l);
+        const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
+        const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+        if constexpr (VS == S_BF16) {
+          const int mi = lane >> 3, rr = lane & 7;
+          const uint8_t* base = vbh + ((mi >> 1) * 8 + rr) * VT::VRS + (mi & 1) * 16;
+#pragma unroll
+          for (int i = 0; i < NK; ++i) {
+            uint32_t f[4];
+            tc::ldsm_x4_t(f, base + i * 32);
+            tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0h, b1h);
+            tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0l, b1l);
+          }
+        } else {  // FP8: tokens 2c, 2c+1, 2c+8, 2c+9; dims g*DPT .. g*DPT + DPT - 1
+          constexpr int DPT = HD / 8;
+          constexpr int W = DPT / 4;  // 32-bit words per token
+          uint32_t w[4][W];
+          const int toks[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint8_t* src = vbh + toks[t] * VT::VRS + g * DPT;
+            if constexpr (W == 2) {
+              const uint2 v = *reinterpret_cast<const uint2*>(src);
+              w[t][0] = v.x; w[t][1] = v.y;
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < W / 4; ++q4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + q4 * 16);
+                w[t][4 * q4] = v.x; w[t][4 * q4 + 1] = v.y; w[t][4 * q4 + 2] = v.z; w[t][4 * q4 + 3] = v.w;
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NK; ++i) {
+            const int wi = (2 * i) / 4;
+            const uint32_t sel = ((2 * i) % 4 == 0) ? 0x5140u : 0x7362u;
+            const uint32_t x01 = tc::prmt(w[0][wi], w[1][wi], sel);   // (t0,t1) @ dims 2i, 2i+1
+            const uint32_t x23 = tc::prmt(w[2][wi], w[3][wi], sel);   // (t2,t3)
+            const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
+            const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
+            tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
+            tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
+          }
+        }
+      } else if constexpr (VT::CB) {
+        // Codebook V: m-tile i is scale group i.  The operand is (level hi,
+        // level lo) x group scale of its token, exact in fp16 (7-bit level
+        // parts, 4-bit scale significand), so P is split once per slab.  Rows
+        // g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1; k-slots are
+        // tokens 2c, 2c+1, 2c+8, 2c+9.
+        uint32_t x1h, x1l, x2h, x2l;
+        tc::split2<false>(p00, p01, x1h, x1l);
+        tc::split2<false>(p10, p11, x2h, x2l);
+        const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
+        const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+        const uint8_t* r0 = vbh + (2 * c) * VT::VRS;
+        const uint8_t* r1 = vbh + (2 * c + 1) * VT::VRS;
+        const uint8_t* r2 = vbh + (2 * c + 8) * VT::VRS;
+        const uint8_t* r3 = vbh + (2 * c + 9) * VT::VRS;
+        const uint8_t* vsc = vsbh;
+        constexpr int SW = (VT::SROW + 3) / 4;   // 32-bit words of a scale row
+        uint32_t s0[SW], s1[SW], s2[SW], s3[SW];
+#pragma unroll
+        for (int q4 = 0; q4 < SW; ++q4) {
+          s0[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c) * VT::SROW + 4 * q4);
+          s1[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 1) * VT::SROW + 4 * q4);
+          s2[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 8) * VT::SROW + 4 * q4);
+          s3[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 9) * VT::SROW + 4 * q4);
+        }
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+          constexpr int B = code_bits(VS);
+          const int bit = B * (16 * i + 2 * g);
+          const uint2 e0 = lut_pair(lut_v, code_pair<B>(r0, bit), lane);
+          const uint2 e1 = lut_pair(lut_v, code_pair<B>(r1, bit), lane);
+          const uint2 e2 = lut_pair(lut_v, code_pair<B>(r2, bit), lane);
+          const uint2 e3 = lut_pair(lut_v, code_pair<B>(r3, bit), lane);
+          // group scales of the four tokens as fp16 pairs (t0,t1), (t2,t3)
+          const uint32_t bsel = (uint32_t)(i & 3) | ((uint32_t)(4 + (i & 3)) << 4);
+          const uint32_t sc01 = tc::e4m3x2_f16x2(tc::prmt(s0[i >> 2], s1[i >> 2], bsel));
+          const uint32_t sc23 = tc::e4m3x2_f16x2(tc::prmt(s2[i >> 2], s3[i >> 2], bsel));
+          // regroup (dim, dim+1) pairs of one token into (token, token) pairs
+          const uint32_t h0 = tc::hmul2(tc::prmt(e0.x, e1.x, 0x5410u), sc01);
+          const uint32_t h2 = tc::hmul2(tc::prmt(e0.x, e1.x, 0x7632u), sc01);
+          const uint32_t h4 = tc::hmul2(tc::prmt(e2.x, e3.x, 0x5410u), sc23);
+          const uint32_t h6 = tc::hmul2(tc::prmt(e2.x, e3.x, 0x7632u), sc23);
+          const uint32_t l0_ = tc::hmul2(tc::prmt(e0.y, e1.y, 0x5410u), sc01);
+          const uint32_t l2_ = tc::hmul2(tc::prmt(e0.y, e1.y, 0x7632u), sc01);
+          const uint32_t l4_ = tc::hmul2(tc::prmt(e2.y, e3.y, 0x5410u), sc23);
+          const uint32_t l6_ = tc::hmul2(tc::prmt(e2.y, e3.y, 0x7632u), sc23);
+          tc::mma<false>(o[i], h0, h2, h4, h6, b0h, b1h);
+          tc::mma<false>(o[i], h0, h2, h4, h6, b0l, b1l);
+          tc::mma<false>(o[i], l0_, l2_, l4_, l6_, b0h, b1h);
+        }
+      } else {
+        // Turbo8 V: m-tile i is scale group i; P is scaled per token by its
+        // BF16 group scale before the split (E4M3 x BF16 is not exact in
+        // fp16).  Rows g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1;
+        // k-slots are tokens 2c, 2c+1, 2c+8, 2c+9.
+        const uint8_t* vsa = vsbh + g * VT::SROW;
+        const uint8_t* vsb = vsbh + (g + 8) * VT::SROW;
+        const uint8_t* r0 = vbh + (2 * c) * VT::VRS;
+        const uint8_t* r1 = vbh + (2 * c + 1) * VT::VRS;
+        const uint8_t* r2 = vbh + (2 * c + 8) * VT::VRS;
+        const uint8_t* r3 = vbh + (2 * c + 9) * VT::VRS;
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+          const float ga = tc_group_scale<VS>(vsa, i), gb = tc_group_scale<VS>(vsb, i);
+          uint32_t x1h, x1l, x2h, x2l;
+          tc::split2<false>(p00 * ga, p01 * ga, x1h, x1l);
+          tc::split2<false>(p10 * gb, p11 * gb, x2h, x2l);
+          const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
+          const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+          {
+            const int off = 16 * i + 2 * g;
+            const uint32_t u0 = *reinterpret_cast<const uint16_t*>(r0 + off);
+            const uint32_t u1 = *reinterpret_cast<const uint16_t*>(r1 + off);
+            const uint32_t u2 = *reinterpret_cast<const uint16_t*>(r2 + off);
+            const uint32_t u3 = *reinterpret_cast<const uint16_t*>(r3 + off);
+            const uint32_t x01 = tc::prmt(u0, u1, 0x5140u);   // (t0,t1) @ dims 2g, 2g+1
+            const uint32_t x23 = tc::prmt(u2, u3, 0x5140u);
+            const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
+            const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
+            tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
+            tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
+          }
+        }
+      }
+  };
+
   for (int s = 0; s < my; ++s) {
     cp_async_wait<C::NST - 2>();
     __syncwarp();
     if (s + C::NST - 1 < my) issue(s + C::NST - 1);
     cp_async_commit();
     const uint8_t* sb = ring + (s % C::NST) * C::STAGE;
-    const uint8_t* kb = sb;
-    const uint8_t* vb = sb + C::OFF_V;
+    const int slab_pos = tok0 + (warp + NW * s) * SLAB;
 
-    // ---- S^T = K . Q^T
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-    float sacl[4] = {0.f, 0.f, 0.f, 0.f};   // second, independent MMA chain
-    if constexpr (KS == S_BF16) {
-      const int mi = lane >> 3, rr = lane & 7;
-      const uint8_t* base = kb + ((mi & 1) * 8 + rr) * KT::KRS + (mi >> 1) * 16;
+    // ---- scores of both row tiles; this thread holds rows g, g+8 of each
+    constexpr int NH = C::NH;
+    float sv[2][4] = {{-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F},
+                      {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F}};
 #pragma unroll
-      for (int j = 0; j < NK; ++j) {
-        uint32_t f[4];
-        tc::ldsm_x4(f, base + j * 32);
-        tc::mma<true>(sacc, f[0], f[1], f[2], f[3], qh[j][0], qh[j][1]);
-        tc::mma<true>(sacl, f[0], f[1], f[2], f[3], ql[j][0], ql[j][1]);
-      }
-    } else if constexpr (KS == S_FP8) {  // thread c converts 16-byte chunks 4jj + c of rows g, g+8
-#pragma unroll
-      for (int jj = 0; jj < NK / 4; ++jj) {
-        const uint4 ra = *reinterpret_cast<const uint4*>(kb + g * KT::KRS + (4 * jj + c) * 16);
-        const uint4 rb = *reinterpret_cast<const uint4*>(kb + (g + 8) * KT::KRS + (4 * jj + c) * 16);
-        const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
-        const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 4 * jj + e;
-          const uint32_t a0 = tc::e4m3x2_f16x2(wa[e] & 0xffffu), a4 = tc::e4m3x2_f16x2(wa[e] >> 16);
-          const uint32_t a2 = tc::e4m3x2_f16x2(wb[e] & 0xffffu), a6 = tc::e4m3x2_f16x2(wb[e] >> 16);
-          tc::mma<false>(sacc, a0, a2, a4, a6, qh[j][0], qh[j][1]);
-          tc::mma<false>(sacl, a0, a2, a4, a6, ql[j][0], ql[j][1]);
-        }
-      }
-    } else {  // group-scaled sides: k-step j is scale group j
-      const uint8_t* ra = kb + g * KT::KRS;
-      const uint8_t* rb = kb + (g + 8) * KT::KRS;
-      const uint8_t* sa = kb + C::OFF_KS + g * KT::SROW;
-      const uint8_t* sbr = kb + C::OFF_KS + (g + 8) * KT::SROW;
-#pragma unroll
-      for (int j = 0; j < NK; ++j) {
-        float cg[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (KS == S_T8) {
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(ra + 16 * j + 4 * c);
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(rb + 16 * j + 4 * c);
-          const uint32_t a0 = tc::e4m3x2_f16x2(wa & 0xffffu), a4 = tc::e4m3x2_f16x2(wa >> 16);
-          const uint32_t a2 = tc::e4m3x2_f16x2(wb & 0xffffu), a6 = tc::e4m3x2_f16x2(wb >> 16);
-          tc::mma<false>(cg, a0, a2, a4, a6, qh[j][0], qh[j][1]);
-          tc::mma<false>(cg, a0, a2, a4, a6, ql[j][0], ql[j][1]);
-        } else {
-          constexpr int B = code_bits(KS);
-          const int bit = B * (16 * j + 4 * c);
-          uint32_t pa0, pa1, pb0, pb1;   // code pairs (dims 4c,4c+1) and (4c+2,4c+3)
-          if constexpr (B == 4) {
-            const uint32_t ua = *reinterpret_cast<const uint16_t*>(ra + (bit >> 3));
-            const uint32_t ub = *reinterpret_cast<const uint16_t*>(rb + (bit >> 3));
-            pa0 = ua & 0xffu; pa1 = ua >> 8; pb0 = ub & 0xffu; pb1 = ub >> 8;
-          } else if constexpr (B == 2) {
-            const uint32_t ua = ra[bit >> 3], ub = rb[bit >> 3];
-            pa0 = ua & 15u; pa1 = ua >> 4; pb0 = ub & 15u; pb1 = ub >> 4;
-          } else {
-            const int sh = bit & 7;
-            const uint32_t ua = ((uint32_t)ra[bit >> 3] | ((uint32_t)ra[(bit >> 3) + 1] << 8)) >> sh;
-            const uint32_t ub = ((uint32_t)rb[bit >> 3] | ((uint32_t)rb[(bit >> 3) + 1] << 8)) >> sh;
-            pa0 = ua & 63u; pa1 = (ua >> 6) & 63u; pb0 = ub & 63u; pb1 = (ub >> 6) & 63u;
-          }
-          const uint2 xa0 = lut_pair(lut_k, pa0, lane);
-          const uint2 xa1 = lut_pair(lut_k, pa1, lane);
-          const uint2 xb0 = lut_pair(lut_k, pb0, lane);
-          const uint2 xb1 = lut_pair(lut_k, pb1, lane);
-          tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, qh[j][0], qh[j][1]);
-          tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
-          tc::mma<false>(cg, xa0.y, xb0.y, xa1.y, xb1.y, qh[j][0], qh[j][1]);
-        }
-        float ga, gb;   // group-j scales of rows g and g+8
-        if constexpr (KS == S_T8) {
-          ga = tc_group_scale<KS>(sa, j);
-          gb = tc_group_scale<KS>(sbr, j);
-        } else {
-          const float2 gs = unpack_f16x2(tc::e4m3x2_f16x2(
-              tc::prmt(*reinterpret_cast<const uint32_t*>(sa + (j & ~3)),
-                       *reinterpret_cast<const uint32_t*>(sbr + (j & ~3)),
-                       (uint32_t)(j & 3) | ((uint32_t)(4 + (j & 3)) << 4))));
-          ga = gs.x;
-          gb = gs.y;
-        }
-        float* acc = (j & 1) ? sacl : sacc;   // two independent accumulators
-        acc[0] = fmaf(cg[0], ga, acc[0]);
-        acc[1] = fmaf(cg[1], ga, acc[1]);
-        acc[2] = fmaf(cg[2], gb, acc[2]);
-        acc[3] = fmaf(cg[3], gb, acc[3]);
-      }
+    for (int h = 0; h < NH; ++h) {
+      float sc4[4];
+      scores16(sb + 16 * h * KT::KRS, sb + C::OFF_KS + 16 * h * KT::SROW, sc4);
+      const bool va = pos_block(slab_pos + 16 * h + g) >= 0;
+      const bool vb_ = pos_block(slab_pos + 16 * h + g + 8) >= 0;
+      sv[h][0] = va ? sc4[0] * scale : -CUDART_INF_F;
+      sv[h][1] = va ? sc4[1] * scale : -CUDART_INF_F;
+      sv[h][2] = vb_ ? sc4[2] * scale : -CUDART_INF_F;
+      sv[h][3] = vb_ ? sc4[3] * scale : -CUDART_INF_F;
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sacc[e] += sacl[e];
 
-    // ---- online softmax; this thread holds rows (tokens) g, g+8, cols 2c, 2c+1
-    const int slab_pos = tok0 + (warp + NW * s) * 16;
-    const bool va = pos_block(slab_pos + g) >= 0;
-    const bool vb_ = pos_block(slab_pos + g + 8) >= 0;
-    const float s00 = va ? sacc[0] * scale : -CUDART_INF_F;
-    const float s01 = va ? sacc[1] * scale : -CUDART_INF_F;
-    const float s10 = vb_ ? sacc[2] * scale : -CUDART_INF_F;
-    const float s11 = vb_ ? sacc[3] * scale : -CUDART_INF_F;
-    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+    // ---- online softmax over the slab's positions (cols 2c, 2c+1)
+    float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2]));
+    float mx1 = fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]));
 #pragma unroll
     for (int msk = 4; msk < 32; msk <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, msk));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, msk));
     }
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    float al0 = 1.f, al1 = 1.f, p00 = 0.f, p10 = 0.f, p01 = 0.f, p11 = 0.f;
+    float al0 = 1.f, al1 = 1.f;
+    float pw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (mn0 != -CUDART_INF_F) {
       al0 = exp2f(m0 - mn0);
-      p00 = exp2f(s00 - mn0);
-      p10 = exp2f(s10 - mn0);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        pw[h][0] = exp2f(sv[h][0] - mn0);
+        pw[h][2] = exp2f(sv[h][2] - mn0);
+      }
     }
     if (mn1 != -CUDART_INF_F) {
       al1 = exp2f(m1 - mn1);
-      p01 = exp2f(s01 - mn1);
-      p11 = exp2f(s11 - mn1);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        pw[h][1] = exp2f(sv[h][1] - mn1);
+        pw[h][3] = exp2f(sv[h][3] - mn1);
+      }
     }
-    l0 = l0 * al0 + p00 + p10;
-    l1 = l1 * al1 + p01 + p11;
+    l0 = l0 * al0 + (pw[0][0] + pw[0][2]) + (pw[1][0] + pw[1][2]);
+    l1 = l1 * al1 + (pw[0][1] + pw[0][3]) + (pw[1][1] + pw[1][3]);
     m0 = mn0;
     m1 = mn1;
     if (a.sparse_thr > 0.f) {  // drop weights <= thr x (this warp's running sum)
@@ -571,10 +734,13 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
         t0 += __shfl_xor_sync(0xffffffffu, t0, msk);
         t1 += __shfl_xor_sync(0xffffffffu, t1, msk);
       }
-      if (p00 <= a.sparse_thr * t0) p00 = 0.f;
-      if (p10 <= a.sparse_thr * t0) p10 = 0.f;
-      if (p01 <= a.sparse_thr * t1) p01 = 0.f;
-      if (p11 <= a.sparse_thr * t1) p11 = 0.f;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        if (pw[h][0] <= a.sparse_thr * t0) pw[h][0] = 0.f;
+        if (pw[h][2] <= a.sparse_thr * t0) pw[h][2] = 0.f;
+        if (pw[h][1] <= a.sparse_thr * t1) pw[h][1] = 0.f;
+        if (pw[h][3] <= a.sparse_thr * t1) pw[h][3] = 0.f;
+      }
     }
     if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
@@ -582,140 +748,10 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
         o[i][0] *= al0; o[i][1] *= al1; o[i][2] *= al0; o[i][3] *= al1;
       }
     }
-
-    // ---- O^T += V^T . P^T
-    if constexpr (!VT::GS) {
-      // P^T operand (hi + lo) from the accumulator layout
-      uint32_t x1h, x1l, x2h, x2l;
-      tc::split2<VT::BF>(p00, p01, x1h, x1l);
-      tc::split2<VT::BF>(p10, p11, x2h, x2l);
-      const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
-      const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
-      if constexpr (VS == S_BF16) {
-        const int mi = lane >> 3, rr = lane & 7;
-        const uint8_t* base = vb + ((mi >> 1) * 8 + rr) * VT::VRS + (mi & 1) * 16;
 #pragma unroll
-        for (int i = 0; i < NK; ++i) {
-          uint32_t f[4];
-          tc::ldsm_x4_t(f, base + i * 32);
-          tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0h, b1h);
-          tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0l, b1l);
-        }
-      } else {  // FP8: tokens 2c, 2c+1, 2c+8, 2c+9; dims g*DPT .. g*DPT + DPT - 1
-        constexpr int DPT = HD / 8;
-        constexpr int W = DPT / 4;  // 32-bit words per token
-        uint32_t w[4][W];
-        const int toks[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint8_t* src = vb + toks[t] * VT::VRS + g * DPT;
-          if constexpr (W == 2) {
-            const uint2 v = *reinterpret_cast<const uint2*>(src);
-            w[t][0] = v.x; w[t][1] = v.y;
-          } else {
-#pragma unroll
-            for (int q4 = 0; q4 < W / 4; ++q4) {
-              const uint4 v = *reinterpret_cast<const uint4*>(src + q4 * 16);
-              w[t][4 * q4] = v.x; w[t][4 * q4 + 1] = v.y; w[t][4 * q4 + 2] = v.z; w[t][4 * q4 + 3] = v.w;
-            }
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < NK; ++i) {
-          const int wi = (2 * i) / 4;
-          const uint32_t sel = ((2 * i) % 4 == 0) ? 0x5140u : 0x7362u;
-          const uint32_t x01 = tc::prmt(w[0][wi], w[1][wi], sel);   // (t0,t1) @ dims 2i, 2i+1
-          const uint32_t x23 = tc::prmt(w[2][wi], w[3][wi], sel);   // (t2,t3)
-          const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
-          const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
-          tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
-          tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
-        }
-      }
-    } else if constexpr (VT::CB) {
-      // Codebook V: m-tile i is scale group i.  The operand is (level hi,
-      // level lo) x group scale of its token, exact in fp16 (7-bit level
-      // parts, 4-bit scale significand), so P is split once per slab.  Rows
-      // g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1; k-slots are
-      // tokens 2c, 2c+1, 2c+8, 2c+9.
-      uint32_t x1h, x1l, x2h, x2l;
-      tc::split2<false>(p00, p01, x1h, x1l);
-      tc::split2<false>(p10, p11, x2h, x2l);
-      const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
-      const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
-      const uint8_t* r0 = vb + (2 * c) * VT::VRS;
-      const uint8_t* r1 = vb + (2 * c + 1) * VT::VRS;
-      const uint8_t* r2 = vb + (2 * c + 8) * VT::VRS;
-      const uint8_t* r3 = vb + (2 * c + 9) * VT::VRS;
-      const uint8_t* vsc = vb + (C::OFF_VS - C::OFF_V);
-      constexpr int SW = (VT::SROW + 3) / 4;   // 32-bit words of a scale row
-      uint32_t s0[SW], s1[SW], s2[SW], s3[SW];
-#pragma unroll
-      for (int q4 = 0; q4 < SW; ++q4) {
-        s0[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c) * VT::SROW + 4 * q4);
-        s1[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 1) * VT::SROW + 4 * q4);
-        s2[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 8) * VT::SROW + 4 * q4);
-        s3[q4] = *reinterpret_cast<const uint32_t*>(vsc + (2 * c + 9) * VT::SROW + 4 * q4);
-      }
-#pragma unroll
-      for (int i = 0; i < NK; ++i) {
-        constexpr int B = code_bits(VS);
-        const int bit = B * (16 * i + 2 * g);
-        const uint2 e0 = lut_pair(lut_v, code_pair<B>(r0, bit), lane);
-        const uint2 e1 = lut_pair(lut_v, code_pair<B>(r1, bit), lane);
-        const uint2 e2 = lut_pair(lut_v, code_pair<B>(r2, bit), lane);
-        const uint2 e3 = lut_pair(lut_v, code_pair<B>(r3, bit), lane);
-        // group scales of the four tokens as fp16 pairs (t0,t1), (t2,t3)
-        const uint32_t bsel = (uint32_t)(i & 3) | ((uint32_t)(4 + (i & 3)) << 4);
-        const uint32_t sc01 = tc::e4m3x2_f16x2(tc::prmt(s0[i >> 2], s1[i >> 2], bsel));
-        const uint32_t sc23 = tc::e4m3x2_f16x2(tc::prmt(s2[i >> 2], s3[i >> 2], bsel));
-        // regroup (dim, dim+1) pairs of one token into (token, token) pairs
-        const uint32_t h0 = tc::hmul2(tc::prmt(e0.x, e1.x, 0x5410u), sc01);
-        const uint32_t h2 = tc::hmul2(tc::prmt(e0.x, e1.x, 0x7632u), sc01);
-        const uint32_t h4 = tc::hmul2(tc::prmt(e2.x, e3.x, 0x5410u), sc23);
-        const uint32_t h6 = tc::hmul2(tc::prmt(e2.x, e3.x, 0x7632u), sc23);
-        const uint32_t l0_ = tc::hmul2(tc::prmt(e0.y, e1.y, 0x5410u), sc01);
-        const uint32_t l2_ = tc::hmul2(tc::prmt(e0.y, e1.y, 0x7632u), sc01);
-        const uint32_t l4_ = tc::hmul2(tc::prmt(e2.y, e3.y, 0x5410u), sc23);
-        const uint32_t l6_ = tc::hmul2(tc::prmt(e2.y, e3.y, 0x7632u), sc23);
-        tc::mma<false>(o[i], h0, h2, h4, h6, b0h, b1h);
-        tc::mma<false>(o[i], h0, h2, h4, h6, b0l, b1l);
-        tc::mma<false>(o[i], l0_, l2_, l4_, l6_, b0h, b1h);
-      }
-    } else {
-      // Turbo8 V: m-tile i is scale group i; P is scaled per token by its
-      // BF16 group scale before the split (E4M3 x BF16 is not exact in
-      // fp16).  Rows g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1;
-      // k-slots are tokens 2c, 2c+1, 2c+8, 2c+9.
-      const uint8_t* vsa = vb + (C::OFF_VS - C::OFF_V) + g * VT::SROW;
-      const uint8_t* vsb = vb + (C::OFF_VS - C::OFF_V) + (g + 8) * VT::SROW;
-      const uint8_t* r0 = vb + (2 * c) * VT::VRS;
-      const uint8_t* r1 = vb + (2 * c + 1) * VT::VRS;
-      const uint8_t* r2 = vb + (2 * c + 8) * VT::VRS;
-      const uint8_t* r3 = vb + (2 * c + 9) * VT::VRS;
-#pragma unroll
-      for (int i = 0; i < NK; ++i) {
-        const float ga = tc_group_scale<VS>(vsa, i), gb = tc_group_scale<VS>(vsb, i);
-        uint32_t x1h, x1l, x2h, x2l;
-        tc::split2<false>(p00 * ga, p01 * ga, x1h, x1l);
-        tc::split2<false>(p10 * gb, p11 * gb, x2h, x2l);
-        const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
-        const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
-        {
-          const int off = 16 * i + 2 * g;
-          const uint32_t u0 = *reinterpret_cast<const uint16_t*>(r0 + off);
-          const uint32_t u1 = *reinterpret_cast<const uint16_t*>(r1 + off);
-          const uint32_t u2 = *reinterpret_cast<const uint16_t*>(r2 + off);
-          const uint32_t u3 = *reinterpret_cast<const uint16_t*>(r3 + off);
-          const uint32_t x01 = tc::prmt(u0, u1, 0x5140u);   // (t0,t1) @ dims 2g, 2g+1
-          const uint32_t x23 = tc::prmt(u2, u3, 0x5140u);
-          const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
-          const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
-          tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
-          tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
-        }
-      }
-    }
+    for (int h = 0; h < NH; ++h)
+      pv16(sb + C::OFF_V + 16 * h * VT::VRS, sb + C::OFF_VS + 16 * h * VT::SROW, pw[h][0],
+           pw[h][1], pw[h][2], pw[h][3]);
   }
   cp_async_wait<0>();
 
