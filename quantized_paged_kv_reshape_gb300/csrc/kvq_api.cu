@@ -297,6 +297,8 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
   if (hd != 64 && hd != 128 && hd != 256) return fail(KVQ_ERR_SHAPE, "head_dim %d not in {64,128,256}", hd);
   if (nkv < 1 || bs < 1) return fail(KVQ_ERR_SHAPE, "num_kv_heads and block_size must be >= 1");
   if (num_tokens == 0) return ok();
+  if ((int64_t)num_tokens * nkv * 2 >= (int64_t)1 << 31)
+    return fail(KVQ_ERR_SHAPE, "num_tokens * num_kv_heads * 2 must be below 2^31 (split the call)");
   if (!key || !value || !k_cache || !v_cache || !slot_mapping) return fail(KVQ_ERR_ARG, "null pointer");
   if (key_stride < (int64_t)nkv * hd || value_stride < (int64_t)nkv * hd)
     return fail(KVQ_ERR_ARG, "key/value stride smaller than num_kv_heads*head_dim");
@@ -323,6 +325,7 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
   a.num_slots = num_blocks * bs;
   a.nkv = nkv;
   a.bs = bs;
+  a.bs_shift = (bs & (bs - 1)) == 0 ? __builtin_ctz((unsigned)bs) : -1;
   a.key_stride = key_stride;
   a.value_stride = value_stride;
   a.k_bstride = k_bstride;
@@ -337,7 +340,7 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
   a.err = error_flag;
   const int64_t rows = (int64_t)num_tokens * nkv * 2;
   const int sms = sm_count();
-  const int64_t want = (rows + 7) / 8;
+  const int64_t want = (rows + 31) / 32;   // 8 warps x 4 rows per CTA iteration
   const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 32;
   const int grid = (int)(want < cap ? want : cap);
   cudaError_t e = launch_cache_write(a, cb, hd, bf, vec, grid, (cudaStream_t)stream);

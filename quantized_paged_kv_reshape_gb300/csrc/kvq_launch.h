@@ -20,6 +20,7 @@ struct WriteArgs {
   int64_t num_slots;      // num_blocks * block_size, 0 = unchecked
   int32_t nkv;
   int32_t bs;
+  int32_t bs_shift;                     // log2(bs) if bs is a power of two, else -1
   int64_t key_stride, value_stride;     // elements per token
   int64_t k_bstride, v_bstride;         // bytes per block
   int64_t k_dsec, v_dsec;               // scale-section offsets

@@ -134,95 +134,136 @@ __device__ __forceinline__ void write_turbo(float (&y)[HD / 32], const float lv_
   if ((lane % LPG) == 0) row_scales[lane / LPG] = sbyte;
 }
 
-template <int HD, typename InT, bool VEC>
-__global__ void __launch_bounds__(256)
-cache_write_kernel(const WriteArgs a, const Codebooks cb) {
+// Encode and store one row already loaded into x (lane's E elements).
+template <int HD>
+__device__ __forceinline__ void write_row(const WriteArgs& a, const Codebooks& cb, int side, int64_t slot,
+                                          int h, float (&x)[HD / 32], int lane) {
   constexpr int E = HD / 32;
-  const int lane = threadIdx.x & 31;
-  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t rows = (int64_t)a.num_tokens * a.nkv * 2;
-  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
-       row += warps_total) {
-    const int64_t t = row / (2 * a.nkv);
-    const int rem = (int)(row - t * 2 * a.nkv);
-    const int side = rem >= a.nkv;
-    const int h = rem - side * a.nkv;
-    const int64_t slot = a.slots[t];
-    if (slot < 0) continue;
-    if (a.num_slots > 0 && slot >= a.num_slots) {
-      if (lane == 0 && a.err) atomicOr(a.err, 1);
-      continue;
-    }
-    const int64_t blk = slot / a.bs;
-    const int off = (int)(slot - blk * a.bs);
-    const int fmt = side ? a.v_side : a.k_side;
-    const InT* src = reinterpret_cast<const InT*>(side ? a.value : a.key) +
-                     t * (side ? a.value_stride : a.key_stride) + (int64_t)h * HD + lane * E;
-    uint8_t* base = (side ? a.v_cache : a.k_cache) + blk * (side ? a.v_bstride : a.k_bstride);
-    const int64_t dsec = side ? a.v_dsec : a.k_dsec;
-    const int64_t ridx = (int64_t)off * a.nkv + h;   // row index inside the block
-
-    float x[E];
-    load_row<E, InT, VEC>(src, x);
-
-    if (fmt == S_BF16) {
-      uint32_t w[(E + 1) / 2];
+  int64_t blk;
+  int off;
+  if (a.bs_shift >= 0) {          // power-of-two block size
+    blk = slot >> a.bs_shift;
+    off = (int)(slot & (a.bs - 1));
+  } else if (slot < 0xffffffffll) {   // 32-bit division
+    const uint32_t s32 = (uint32_t)slot;
+    blk = s32 / (uint32_t)a.bs;
+    off = (int)(s32 - (uint32_t)blk * (uint32_t)a.bs);
+  } else {
+    blk = slot / a.bs;
+    off = (int)(slot - blk * a.bs);
+  }
+  const int fmt = side ? a.v_side : a.k_side;
+  uint8_t* base = (side ? a.v_cache : a.k_cache) + blk * (side ? a.v_bstride : a.k_bstride);
+  const int64_t dsec = side ? a.v_dsec : a.k_dsec;
+  const int64_t ridx = (int64_t)off * a.nkv + h;   // row index inside the block
+  if (fmt == S_BF16) {
+    uint32_t w[(E + 1) / 2];
 #pragma unroll
-      for (int i = 0; i < E; i += 2)
-        w[i / 2] = (uint32_t)bf16_bits_from_float(x[i]) |
-                   ((uint32_t)bf16_bits_from_float(x[i + 1]) << 16);
-      uint8_t* dst = base + (ridx * HD + lane * E) * 2;
-      if constexpr (E == 2) store_bytes<4>(dst, w[0]);
-      else if constexpr (E == 4) store_bytes<8>(dst, w[0], w[1]);
-      else *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else if (fmt == S_FP8) {
-      const float sc = side ? a.v_scale : a.k_scale;
+    for (int i = 0; i < E; i += 2)
+      w[i / 2] = (uint32_t)bf16_bits_from_float(x[i]) |
+                 ((uint32_t)bf16_bits_from_float(x[i + 1]) << 16);
+    uint8_t* dst = base + (ridx * HD + lane * E) * 2;
+    if constexpr (E == 2) store_bytes<4>(dst, w[0]);
+    else if constexpr (E == 4) store_bytes<8>(dst, w[0], w[1]);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if (fmt == S_FP8) {
+    const float sc = side ? a.v_scale : a.k_scale;
+    uint32_t w[(E + 3) / 4] = {};
+#pragma unroll
+    for (int i = 0; i < E; ++i) w[i / 4] |= (uint32_t)e4m3_from_float(x[i] / sc) << (8 * (i % 4));
+    uint8_t* dst = base + ridx * HD + lane * E;
+    if constexpr (E == 2) store_bytes<2>(dst, w[0]);
+    else if constexpr (E == 4) store_bytes<4>(dst, w[0]);
+    else store_bytes<8>(dst, w[0], w[1]);
+  } else {
+    fwht_warp<E>(x, lane, a.inv_sqrt_hd);
+    if (fmt == S_T8) {
+      const float amax = group_amax<E>(x);
+      const uint16_t sbits = bf16_bits_from_float(amax / 448.0f);
+      const float s = bf16_bits_to_float(sbits);
       uint32_t w[(E + 3) / 4] = {};
 #pragma unroll
-      for (int i = 0; i < E; ++i) w[i / 4] |= (uint32_t)e4m3_from_float(x[i] / sc) << (8 * (i % 4));
+      for (int i = 0; i < E; ++i) {
+        const uint32_t b = s == 0.f ? 0u : (uint32_t)e4m3_from_float(x[i] / s);
+        w[i / 4] |= b << (8 * (i % 4));
+      }
       uint8_t* dst = base + ridx * HD + lane * E;
       if constexpr (E == 2) store_bytes<2>(dst, w[0]);
       else if constexpr (E == 4) store_bytes<4>(dst, w[0]);
       else store_bytes<8>(dst, w[0], w[1]);
+      constexpr int LPG = kGroup / E;
+      if ((lane % LPG) == 0)
+        store_bytes<2>(base + dsec + (ridx * (HD / kGroup) + lane / LPG) * 2, sbits);
+    } else if (fmt == S_T4) {
+      float th[15];
+#pragma unroll
+      for (int i = 0; i < 15; ++i) th[i] = cb.th4[i];
+      write_turbo<HD, 4>(x, cb.lv4[15], th, base + ridx * (HD / 2),
+                         base + dsec + ridx * (HD / kGroup), lane);
+    } else if (fmt == S_T3) {
+      float th[7];
+#pragma unroll
+      for (int i = 0; i < 7; ++i) th[i] = cb.th3[i];
+      write_turbo<HD, 3>(x, cb.lv3[7], th, base + ridx * (HD * 3 / 8),
+                         base + dsec + ridx * (HD / kGroup), lane);
     } else {
-      fwht_warp<E>(x, lane, a.inv_sqrt_hd);
-      if (fmt == S_T8) {
-        const float amax = group_amax<E>(x);
-        const uint16_t sbits = bf16_bits_from_float(amax / 448.0f);
-        const float s = bf16_bits_to_float(sbits);
-        uint32_t w[(E + 3) / 4] = {};
+      float th[3];
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
-          const uint32_t b = s == 0.f ? 0u : (uint32_t)e4m3_from_float(x[i] / s);
-          w[i / 4] |= b << (8 * (i % 4));
-        }
-        uint8_t* dst = base + ridx * HD + lane * E;
-        if constexpr (E == 2) store_bytes<2>(dst, w[0]);
-        else if constexpr (E == 4) store_bytes<4>(dst, w[0]);
-        else store_bytes<8>(dst, w[0], w[1]);
-        constexpr int LPG = kGroup / E;
-        if ((lane % LPG) == 0)
-          store_bytes<2>(base + dsec + (ridx * (HD / kGroup) + lane / LPG) * 2, sbits);
-      } else if (fmt == S_T4) {
-        float th[15];
+      for (int i = 0; i < 3; ++i) th[i] = cb.th2[i];
+      write_turbo<HD, 2>(x, cb.lv2[3], th, base + ridx * (HD / 4),
+                         base + dsec + ridx * (HD / kGroup), lane);
+    }
+  }
+}
+
+// Each warp takes RB consecutive rows per iteration (row = (token, side,
+// kv head), heads fastest): the slot and input loads of all RB rows are
+// issued before any row is encoded, so every warp keeps RB rows of loads in
+// flight.
+template <int HD, typename InT, bool VEC>
+__global__ void __launch_bounds__(256)
+cache_write_kernel(const WriteArgs a, const Codebooks cb) {
+  constexpr int E = HD / 32;
+  constexpr int RB = HD == 256 ? 2 : 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t rows = (int64_t)a.num_tokens * a.nkv * 2;
+  for (int64_t row0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RB;
+       row0 < rows; row0 += warps_total * RB) {
+    int64_t slot[RB];
+    int side[RB], head[RB];
+    float x[RB][E];
+    // The input row's address does not depend on its slot, so slot and input
+    // loads of all RB rows issue back to back (rows past the end re-read
+    // the last row and are dropped).
+    // rows fit 32 bits (checked on the host): one division per batch
+    const uint32_t rpt = 2u * (uint32_t)a.nkv;                 // rows per token
+    const uint32_t rlast = (uint32_t)(rows - 1);
+    const uint32_t r0 = (uint32_t)row0;
+    uint32_t t0 = r0 / rpt;
+    uint32_t rem0 = r0 - t0 * rpt;
 #pragma unroll
-        for (int i = 0; i < 15; ++i) th[i] = cb.th4[i];
-        write_turbo<HD, 4>(x, cb.lv4[15], th, base + ridx * (HD / 2),
-                           base + dsec + ridx * (HD / kGroup), lane);
-      } else if (fmt == S_T3) {
-        float th[7];
+    for (int r = 0; r < RB; ++r) {
+      uint32_t t = t0, rem = rem0 + r;
+      while (rem >= rpt) { rem -= rpt; ++t; }                   // at most RB/rpt steps
+      if (r0 + r > rlast) { t = rlast / rpt; rem = rlast - t * rpt; }
+      side[r] = (int)rem >= a.nkv;
+      head[r] = rem - side[r] * a.nkv;
+      slot[r] = row0 + r < rows ? a.slots[t] : -1;
+      const InT* src = reinterpret_cast<const InT*>(side[r] ? a.value : a.key) +
+                       t * (side[r] ? a.value_stride : a.key_stride) + (int64_t)head[r] * HD + lane * E;
+      load_row<E, InT, VEC>(src, x[r]);
+    }
 #pragma unroll
-        for (int i = 0; i < 7; ++i) th[i] = cb.th3[i];
-        write_turbo<HD, 3>(x, cb.lv3[7], th, base + ridx * (HD * 3 / 8),
-                           base + dsec + ridx * (HD / kGroup), lane);
-      } else {
-        float th[3];
-#pragma unroll
-        for (int i = 0; i < 3; ++i) th[i] = cb.th2[i];
-        write_turbo<HD, 2>(x, cb.lv2[3], th, base + ridx * (HD / 4),
-                           base + dsec + ridx * (HD / kGroup), lane);
+    for (int r = 0; r < RB; ++r) {
+      if (slot[r] >= 0 && a.num_slots > 0 && slot[r] >= a.num_slots) {
+        if (lane == 0 && a.err) atomicOr(a.err, 1);
+        slot[r] = -1;
       }
     }
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+      if (slot[r] >= 0) write_row<HD>(a, cb, side[r], slot[r], head[r], x[r], lane);
   }
 }
 
