@@ -146,8 +146,8 @@ struct SplitPlan {
 
 // Flash-decoding split: enough CTAs of (split, kv head, sequence) to fill the
 // SMs several times, each split at least two 32-token tiles long.
-// ctas_per_sm: 3 for the tensor-core kernel (long splits amortize its
-// prologue and merge), 6 for the CUDA-core kernel (measured on GB300).
+// ctas_per_sm = 3 (measured on GB300: long splits amortize the decode
+// kernel's prologue and merge).
 SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, int sms,
                      int ctas_per_sm) {
   const int tp = 32 / bs;
@@ -169,25 +169,11 @@ SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, 
   return {nsplit, pps};
 }
 
-int split_ctas_per_sm(kvq_format fmt) {
-  return decode_tc_supported(side_of(fmt, 0), side_of(fmt, 1)) ? 3 : 6;
-}
+int split_ctas_per_sm(kvq_format) { return 3; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 int rmax_for(int rep) { return rep <= 1 ? 1 : rep <= 2 ? 2 : rep <= 4 ? 4 : rep <= 8 ? 8 : 0; }
-
-size_t decode_smem(int ks, int vs, int hd, int rmax) {
-  switch (ks) {
-    case S_BF16: return smem_k_bf16(vs, hd, rmax);
-    case S_FP8: return smem_k_fp8(vs, hd, rmax);
-    case S_T4: return smem_k_t4(vs, hd, rmax);
-    case S_T3: return smem_k_t3(vs, hd, rmax);
-    case S_T2: return smem_k_t2(vs, hd, rmax);
-    case S_T8: return smem_k_t8(vs, hd, rmax);
-    default: return 0;
-  }
-}
 
 }  // namespace
 
@@ -195,22 +181,6 @@ namespace kvq {
 // Lets other translation units of the library report a message through
 // kvq_last_error().
 void record_error(const char* msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
-
-size_t decode_smem_bytes(int k_side, int v_side, int head_dim, int rmax) {
-  return decode_smem(k_side, v_side, head_dim, rmax);
-}
-cudaError_t launch_decode(int ks, int vs, int hd, int rmax, const DecodeArgs& a,
-                          const Codebooks& cb, cudaStream_t st) {
-  switch (ks) {
-    case S_BF16: return launch_decode_k_bf16(vs, hd, rmax, a, cb, st);
-    case S_FP8: return launch_decode_k_fp8(vs, hd, rmax, a, cb, st);
-    case S_T4: return launch_decode_k_t4(vs, hd, rmax, a, cb, st);
-    case S_T3: return launch_decode_k_t3(vs, hd, rmax, a, cb, st);
-    case S_T2: return launch_decode_k_t2(vs, hd, rmax, a, cb, st);
-    case S_T8: return launch_decode_k_t8(vs, hd, rmax, a, cb, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
 }  // namespace kvq
 
 extern "C" {
@@ -399,7 +369,7 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   const size_t need = (size_t)num_seqs * nq * p.nsplit * (hd + 4) * sizeof(float);
   if (workspace_bytes < need)
     return fail(KVQ_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
-  if (decode_smem(ks, vs, hd, rmax) == 0) return fail(KVQ_ERR_FORMAT, "no decode instance for this pair");
+  if (!decode_tc_supported(ks, vs)) return fail(KVQ_ERR_FORMAT, "no decode instance for this pair");
   const Codebooks& cb = codebooks();
   const double scale = sm_scale == 0.f ? 1.0 / std::sqrt((double)hd) : (double)sm_scale;
   DecodeArgs a{};
@@ -431,8 +401,7 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   a.part = (float*)workspace;
   a.err = error_flag;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = decode_tc_supported(ks, vs) ? launch_decode_tc(ks, vs, hd, a, cb, st)
-                                               : launch_decode(ks, vs, hd, rmax, a, cb, st);
+  cudaError_t e = launch_decode_tc(ks, vs, hd, a, cb, st);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   CombineArgs c{};
   c.part = a.part;

@@ -32,7 +32,7 @@
 
 #include <type_traits>
 
-#include "kvq_decode.cuh"
+#include "kvq_decode_common.cuh"
 
 namespace kvq {
 

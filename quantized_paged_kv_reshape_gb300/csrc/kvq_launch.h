@@ -30,7 +30,7 @@ struct WriteArgs {
   int32_t* err;
 };
 
-struct DecodeArgs {
+struct DecodeArgs {  // arguments of the split-K decode (decode_tc_kernel)
   const void* q;
   int64_t q_stride;       // elements between sequences
   int q_bf16;
@@ -67,27 +67,7 @@ struct CombineArgs {
 cudaError_t launch_cache_write(const WriteArgs& a, const Codebooks& cb, int head_dim,
                                bool in_bf16, bool vec, int grid, cudaStream_t st);
 
-// Split-K decode for one (K side, V side) pair; returns cudaErrorInvalidValue
-// for a pair / head_dim / rmax without an instance.
-cudaError_t launch_decode(int k_side, int v_side, int head_dim, int rmax,
-                          const DecodeArgs& a, const Codebooks& cb, cudaStream_t st);
-
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
-
-// Per-K-side entry points, one translation unit each.
-cudaError_t launch_decode_k_bf16(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
-cudaError_t launch_decode_k_fp8(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
-cudaError_t launch_decode_k_t4(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
-cudaError_t launch_decode_k_t3(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
-cudaError_t launch_decode_k_t2(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
-cudaError_t launch_decode_k_t8(int v_side, int hd, int rmax, const DecodeArgs&, const Codebooks&, cudaStream_t);
-size_t smem_k_bf16(int v_side, int hd, int rmax);
-size_t smem_k_fp8(int v_side, int hd, int rmax);
-size_t smem_k_t4(int v_side, int hd, int rmax);
-size_t smem_k_t3(int v_side, int hd, int rmax);
-size_t smem_k_t2(int v_side, int hd, int rmax);
-size_t smem_k_t8(int v_side, int hd, int rmax);
-
 
 // Tensor-core decode (kvq_decode_tc_k_*.cu) for the pairs it supports.
 bool decode_tc_supported(int k_side, int v_side);
@@ -99,8 +79,5 @@ cudaError_t launch_tc_k_t4(int v_side, int hd, const DecodeArgs&, const Codebook
 cudaError_t launch_tc_k_t3(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 cudaError_t launch_tc_k_t2(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 cudaError_t launch_tc_k_t8(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
-
-// Shared memory bytes the decode instance needs (0 if no instance).
-size_t decode_smem_bytes(int k_side, int v_side, int head_dim, int rmax);
 
 }  // namespace kvq
