@@ -40,6 +40,21 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged-decode HBM GB/s (cache bytes read / time), us/layer, cache-write GB/s"
 WORKLOAD = "llama8b"
+WORKLOAD_DESC = {
+    "llama8b": "llama8b decode layer: {nseq} seqs x 4096 ctx, 32 q / 8 kv heads, head_dim 128, "
+               "block_size 16; one layer per format",
+    "ragged": "ragged decode layer: {nseq} seqs, lengths U[512, 16384], 32 q / 8 kv heads, "
+              "head_dim 128, block_size 16",
+    "longctx": "long-context decode layer: {nseq} seqs x 131072, 64 q / 8 kv heads, head_dim 128, "
+               "windows 0 and 4096",
+    "gemma_write": "write-heavy step: 8192-token fused-QKV write (stride 16384) + decode over "
+                   "{nseq} seqs x 8192, 32 q / 16 kv heads, head_dim 256",
+    "tiny": "tiny: {nseq} seqs of 37/50 tokens, 4 q / 2 kv heads, head_dim 64",
+}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# decode launch, from the ncu capture summarised in profiles/ (None when the
+# kernel changed after the capture).
+TRAFFIC = {}
 
 
 def peaks():
@@ -141,32 +156,35 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
     _abi.lib()
 
-    w = W.make(WORKLOAD, seed=rank)
-    if args.num_seqs != w.num_seqs:
-        w = W.make(WORKLOAD, seed=rank, num_seqs=args.num_seqs,
-                   seq_lens=np.full(args.num_seqs, int(w.seq_lens[0]), np.int32))
+    w = W.make(args.workload, seed=rank)
+    if args.num_seqs and args.num_seqs != w.num_seqs:
+        w = W.make(args.workload, seed=rank, num_seqs=args.num_seqs,
+                   seq_lens=np.resize(w.seq_lens, args.num_seqs).astype(np.int32))
     nkv, nq, hd, bs = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size
     nseq = w.num_seqs
-    L = int(w.seq_lens[0])
+    lens_np = np.asarray(w.seq_lens, np.int64)
     tables_np = W.block_tables(w)
     mb = tables_np.shape[1]
     tables = torch.from_numpy(tables_np).to(dev)
     lens = torch.from_numpy(w.seq_lens).to(dev)
     g = torch.Generator(device=dev)
     g.manual_seed(1234 + rank)
+    act = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
 
-    # K/V of every cached position: bf16 N(0,1) * per-channel scale (lognormal
-    # sigma 0.5, 1% of channels x10), drawn on the device.
+    # K/V of every cached position, drawn on the device with the workload's
+    # distribution (per-channel scale, outlier channels).
     ch_k = torch.from_numpy(W.channel_scales(w, 0)).to(dev)
     ch_v = torch.from_numpy(W.channel_scales(w, 1)).to(dev)
-    ntok = nseq * L
+    ntok = int(lens_np.sum())
     slots_all = torch.from_numpy(W.slot_mapping_for_sequences(w, tables_np)).to(dev)
-    kall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_k).to(torch.bfloat16)
-    vall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_v).to(torch.bfloat16)
+    kall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_k).to(act)
+    vall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_v).to(act)
     k_scale = float(kall.float().abs().amax()) / 448.0
     v_scale = float(vall.float().abs().amax()) / 448.0
+    in_bytes = 2 if act == torch.bfloat16 else 4
 
     fmts = [f for f in w.formats if f in args.formats.split(",")] if args.formats else list(w.formats)
+    windows = list(w.windows)
     pools = {}
     write_ms = {}
     for f in fmts:
@@ -184,31 +202,59 @@ def run_gpu(args):
             if rep:
                 write_ms.setdefault(f, []).append(e0.elapsed_time(e1))
 
-    # Step inputs: the new token of every sequence (position L-1) and its query.
-    q = (torch.randn((nseq, nq, hd), generator=g, device=dev)).to(torch.bfloat16)
-    knew = kall.view(nseq, L, nkv, hd)[:, L - 1].contiguous()
-    vnew = vall.view(nseq, L, nkv, hd)[:, L - 1].contiguous()
-    slots_new = slots_all.view(nseq, L)[:, L - 1].contiguous()
+    # Step inputs: the newest token of every sequence (its last position) and
+    # its query; the write-heavy workload also writes a fused-QKV prefill
+    # chunk scattered over the pool.
+    last = torch.from_numpy(np.cumsum(lens_np) - 1).to(dev)
+    q = torch.randn((nseq, nq, hd), generator=g, device=dev).to(act)
+    knew = kall[last].contiguous()
+    vnew = vall[last].contiguous()
+    slots_new = slots_all[last].contiguous()
+    prefill = None
+    if w.write_tokens:
+        fused = torch.randn((w.write_tokens, w.write_row_elems), generator=g, device=dev).to(act)
+        pslots = torch.from_numpy(W.scattered_slots(w.write_tokens, w.num_blocks, bs)).to(dev)
+        prefill = (fused, pslots)
     outs = {f: torch.empty((nseq, nq, hd), dtype=torch.float32, device=dev) for f in fmts}
-    wsp = {f: ops.alloc_workspace(nseq, nq, nkv, hd, bs, mb, 0, f, device=dev) for f in fmts}
+    wsp = {(f, win): ops.alloc_workspace(nseq, nq, nkv, hd, bs, mb, win, f, device=dev)
+           for f in fmts for win in windows}
     del kall, vall
 
     stream = torch.cuda.current_stream()
-    ev = {f: [] for f in fmts}
+    ev = {(f, win): [] for f in fmts for win in windows}
+    evw = {f: [] for f in fmts}
 
-    def step(record=False):
+    def step(record=False, q_=None, k_=None, v_=None, s_=None, host_out=None):
+        q_ = q if q_ is None else q_
+        k_ = knew if k_ is None else k_
+        v_ = vnew if v_ is None else v_
+        s_ = slots_new if s_ is None else s_
         for f in fmts:
             kp, vp = pools[f]
-            ops.cache_write(knew.view(nseq, -1), vnew.view(nseq, -1), kp, vp, slots_new, f, nkv,
-                            hd, bs, k_scale=k_scale, v_scale=v_scale)
             if record:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-            ops.paged_decode(q, kp, vp, tables, lens, f, nkv, bs, out=outs[f], k_scale=k_scale,
-                             v_scale=v_scale, workspace=wsp[f])
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+            if prefill is not None:
+                fused, pslots = prefill
+                ops.cache_write(fused[:, nq * hd:], fused[:, (nq + nkv) * hd:], kp, vp, pslots, f,
+                                nkv, hd, bs, key_stride=w.write_row_elems,
+                                value_stride=w.write_row_elems, k_scale=k_scale, v_scale=v_scale)
+            ops.cache_write(k_.view(nseq, -1), v_.view(nseq, -1), kp, vp, s_, f, nkv, hd, bs,
+                            k_scale=k_scale, v_scale=v_scale)
             if record:
-                b.record(stream)
-                ev[f].append((a, b))
+                a1.record(stream)
+                evw[f].append((a0, a1))
+            for win in windows:
+                if record:
+                    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    b0.record(stream)
+                ops.paged_decode(q_, kp, vp, tables, lens, f, nkv, bs, out=outs[f], k_scale=k_scale,
+                                 v_scale=v_scale, sliding_window=win, workspace=wsp[(f, win)])
+                if record:
+                    b1.record(stream)
+                    ev[(f, win)].append((b0, b1))
+                if host_out is not None:
+                    host_out[(f, win)].copy_(outs[f], non_blocking=True)
 
     for _ in range(args.warmup):
         step()
@@ -234,29 +280,23 @@ def run_gpu(args):
     clocks = sampler.stop() if rank == 0 else None
 
     # e2e through the public API: pinned host inputs -> device, outputs -> host.
-    h_q = q.cpu().pin_memory()
-    h_k = knew.cpu().pin_memory()
-    h_v = vnew.cpu().pin_memory()
-    h_slots = slots_new.cpu().pin_memory()
-    h_tab = tables.cpu().pin_memory()
-    h_lens = lens.cpu().pin_memory()
-    h_out = {f: torch.empty((nseq, nq, hd), dtype=torch.float32).pin_memory() for f in fmts}
-    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(knew), torch.empty_like(vnew)
-    d_slots, d_tab, d_lens = torch.empty_like(slots_new), torch.empty_like(tables), torch.empty_like(lens)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tab, h_lens))
+    h_in = [t.cpu().pin_memory() for t in (q, knew, vnew, slots_new, tables, lens)]
+    d_in = [torch.empty_like(t) for t in (q, knew, vnew, slots_new, tables, lens)]
+    h_out = {(f, win): torch.empty((nseq, nq, hd), dtype=torch.float32).pin_memory()
+             for f in fmts for win in windows}
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    if prefill is not None:
+        h_fused = prefill[0].cpu().pin_memory()
+        d_fused = torch.empty_like(prefill[0])
+        h2d += h_fused.numel() * h_fused.element_size()
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
     def e2e_step():
-        for src, dst in ((h_q, d_q), (h_k, d_k), (h_v, d_v), (h_slots, d_slots), (h_tab, d_tab),
-                         (h_lens, d_lens)):
+        for src, dst in zip(h_in, d_in):
             dst.copy_(src, non_blocking=True)
-        for f in fmts:
-            kp, vp = pools[f]
-            ops.cache_write(d_k.view(nseq, -1), d_v.view(nseq, -1), kp, vp, d_slots, f, nkv, hd,
-                            bs, k_scale=k_scale, v_scale=v_scale)
-            ops.paged_decode(d_q, kp, vp, d_tab, d_lens, f, nkv, bs, out=outs[f],
-                             k_scale=k_scale, v_scale=v_scale, workspace=wsp[f])
-            h_out[f].copy_(outs[f], non_blocking=True)
+        if prefill is not None:
+            d_fused.copy_(h_fused, non_blocking=True)
+        step(q_=d_in[0], k_=d_in[1], v_=d_in[2], s_=d_in[3], host_out=h_out)
 
     for _ in range(3):
         e2e_step()
@@ -277,38 +317,48 @@ def run_gpu(args):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step, e2e_ms = float(t[0]), float(t[1])
 
-    dec_bytes = {f: algorithmic_decode_bytes(f, w.seq_lens, nkv, hd, bs) for f in fmts}
-    step_bytes = sum(dec_bytes.values()) + sum(write_bytes(f, nseq, nkv, hd, bs) for f in fmts)
+    dec_bytes = {(f, win): algorithmic_decode_bytes(f, w.seq_lens, nkv, hd, bs, win)
+                 for f in fmts for win in windows}
+    wtok = nseq + (w.write_tokens or 0)
+    step_bytes = sum(dec_bytes.values()) + sum(write_bytes(f, wtok, nkv, hd, bs, in_bytes)
+                                               for f in fmts)
     peak, peak_kind = peaks()
-    per_fmt = {}
+    per_layer = {}
+    for (f, win), lst in ev.items():
+        us = statistics.mean(a.elapsed_time(b) for a, b in lst) * 1e3
+        gbs = dec_bytes[(f, win)] / (us * 1e-6) / 1e9
+        key = f if len(windows) == 1 else f"{f}@window{win}"
+        per_layer[key] = {"us_per_layer": round(us, 2), "decode_gbs": round(gbs, 1),
+                          "frac_of_peak": round(gbs / peak, 4), "cache_bytes": dec_bytes[(f, win)]}
+    per_write = {}
     for f in fmts:
-        us = statistics.mean(a.elapsed_time(b) for a, b in ev[f]) * 1e3
-        gbs = dec_bytes[f] / (us * 1e-6) / 1e9
         wms = statistics.mean(write_ms[f])
-        per_fmt[f] = {"us_per_layer": round(us, 2), "decode_gbs": round(gbs, 1),
-                      "frac_of_peak": round(gbs / peak, 4),
-                      "cache_bytes": dec_bytes[f],
-                      "write_gbs": round(write_bytes(f, ntok, nkv, hd, bs) / (wms * 1e-3) / 1e9, 1),
-                      "write_us_131072_tokens": round(wms * 1e3, 1)}
-    dom = max(fmts, key=lambda f: per_fmt[f]["us_per_layer"])
+        us_w = statistics.mean(a.elapsed_time(b) for a, b in evw[f]) * 1e3
+        per_write[f] = {"fill_gbs": round(write_bytes(f, ntok, nkv, hd, bs, in_bytes) / (wms * 1e-3) / 1e9, 1),
+                        "fill_us": round(wms * 1e3, 1), "fill_tokens": ntok,
+                        "step_write_us": round(us_w, 2), "step_write_tokens": wtok,
+                        "step_write_gbs": round(write_bytes(f, wtok, nkv, hd, bs, in_bytes) / (us_w * 1e-6) / 1e9, 1)}
+    dom = max(per_layer, key=lambda k: per_layer[k]["us_per_layer"])
     value = step_bytes * ws / (ms_step * 1e-3) / 1e9
     e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
-    launches_per_step = 3 * len(fmts)   # noqa: E501   # write + decode split + combine per format
+    launches_per_step = len(fmts) * ((2 if prefill is not None else 1) + 2 * len(windows))
+    dom_fmt = dom.split("@")[0]
+    traffic = TRAFFIC.get((args.workload, dom)) if not args.num_seqs or args.num_seqs == W.make(args.workload).num_seqs else None
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"llama8b decode layer: {nseq} seqs x {L} ctx, 32 q / 8 kv heads, "
-                               "head_dim 128, block_size 16; one layer per format",
-                   "formats": fmts,
+        "config": {"workload": WORKLOAD_DESC[args.workload].format(nseq=nseq),
+                   "formats": fmts, "windows": windows,
                    "l2": f"inputs larger than L2 ({sum(dec_bytes.values()) / 1e6:.0f} MB of cache per step)",
                    "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
-        "per_format": per_fmt,
-        "roofline": {"kernel": f"{decode_kernel_name(dom)} ({dom}) + combine_kernel", "bound": "hbm",
-                     "achieved": per_fmt[dom]["decode_gbs"], "peak": peak, "unit": "GB/s",
-                     "frac": round(per_fmt[dom]["decode_gbs"] / peak, 4),
-                     "traffic": None, "peak_kind": peak_kind + " (hbm_gbs copy)",
+        "per_layer": per_layer,
+        "cache_write": per_write,
+        "roofline": {"kernel": f"decode_tc_kernel + combine_kernel ({dom})", "bound": "hbm",
+                     "achieved": per_layer[dom]["decode_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": round(per_layer[dom]["decode_gbs"] / peak, 4),
+                     "traffic": traffic, "peak_kind": peak_kind + " (hbm_gbs copy)",
                      "timed": "split + combine kernels per launch, CUDA events on the launch stream"},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
@@ -405,7 +455,8 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--num-seqs", type=int, default=32, help="sequences of 4096 tokens")
+    ap.add_argument("--num-seqs", type=int, default=0, help="override the number of sequences")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOAD_DESC))
     ap.add_argument("--formats", default="", help="comma list (default bf16,fp8,turbo4)")
     args = ap.parse_args()
     if args.warmup < 3:

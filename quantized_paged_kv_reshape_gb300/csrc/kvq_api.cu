@@ -169,7 +169,10 @@ SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, 
   return {nsplit, pps};
 }
 
-int split_ctas_per_sm(kvq_format) { return 3; }
+#ifndef KVQ_SPLIT_CTAS_PER_SM
+#define KVQ_SPLIT_CTAS_PER_SM 3
+#endif
+int split_ctas_per_sm(kvq_format) { return KVQ_SPLIT_CTAS_PER_SM; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
