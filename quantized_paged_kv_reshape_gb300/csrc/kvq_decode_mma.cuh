@@ -268,7 +268,30 @@ __device__ __forceinline__ uint2 lut_pair(const uint2* lut, uint32_t pair, int l
   return lut[pair * 16 + (lane & 15)];
 }
 
-template <int KS, int VS, int HD>
+// P^T operand of m16n8k16 from this thread's S^T accumulators (rows g,
+// g+8, columns 2c, 2c+1): b[0], b[1] carry the hi parts (k rows 0-7, 8-15)
+// and b[2], b[3] the lo parts.  PK: lanes c < 2 (columns 0-3) contribute
+// hi parts and lanes c >= 2 (columns 4-7) lo parts, so b[0], b[1] carry
+// both and b[2], b[3] are unused.
+template <bool BF, bool PK>
+__device__ __forceinline__ void p_operand(float p00, float p01, float p10, float p11, int c,
+                                          uint32_t (&b)[4]) {
+  uint32_t x1h, x1l, x2h, x2l;
+  tc::split2<BF>(p00, p01, x1h, x1l);
+  tc::split2<BF>(p10, p11, x2h, x2l);
+  if constexpr (PK) {
+    b[0] = tc::movm_t(c < 2 ? x1h : x1l);
+    b[1] = tc::movm_t(c < 2 ? x2h : x2l);
+    b[2] = b[3] = 0u;
+  } else {
+    b[0] = tc::movm_t(x1h);
+    b[1] = tc::movm_t(x2h);
+    b[2] = tc::movm_t(x1l);
+    b[3] = tc::movm_t(x2l);
+  }
+}
+
+template <int KS, int VS, int HD, bool PK>
 __global__ void __launch_bounds__(32 * TcWarps<KS, VS, HD>::NW, 2)
 decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   using C = TcCfg<KS, VS, HD>;
@@ -421,14 +444,25 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     for (int i = 0; i < E; ++i) q_s[j * HD + lane * E + i] = x[i];
   }
   __syncthreads();  // q_s complete (copies of the first slabs are in flight)
-  uint32_t qh[NK][2], ql[NK][2];
+  // Q^T operand (B column n = g).  PK: column g carries head g & 3, its hi
+  // part for g < 4 and its lo part for g >= 4 (qh only); otherwise column g
+  // is head g, with the hi and lo parts in separate operands qh, ql.
+  uint32_t qh[NK][2], ql[PK ? 1 : NK][2];
 #pragma unroll
   for (int j = 0; j < NK; ++j) {
     int d[4];
     k_slot_dims<KS, HD>(j, c, d);
-    const float* qr = q_s + g * HD;
-    tc::split2<KT::BF>(qr[d[0]], qr[d[1]], qh[j][0], ql[j][0]);
-    tc::split2<KT::BF>(qr[d[2]], qr[d[3]], qh[j][1], ql[j][1]);
+    const float* qr = q_s + (PK ? (g & 3) : g) * HD;
+    uint32_t h0, l0, h1, l1;
+    tc::split2<KT::BF>(qr[d[0]], qr[d[1]], h0, l0);
+    tc::split2<KT::BF>(qr[d[2]], qr[d[3]], h1, l1);
+    if constexpr (PK) {
+      qh[j][0] = g < 4 ? h0 : l0;
+      qh[j][1] = g < 4 ? h1 : l1;
+    } else {
+      qh[j][0] = h0; ql[j][0] = l0;
+      qh[j][1] = h1; ql[j][1] = l1;
+    }
   }
 
   float o[NK][4];
@@ -449,8 +483,12 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
         for (int j = 0; j < NK; ++j) {
           uint32_t f[4];
           tc::ldsm_x4(f, base + j * 32);
-          tc::mma<true>(sacc, f[0], f[1], f[2], f[3], qh[j][0], qh[j][1]);
-          tc::mma<true>(sacl, f[0], f[1], f[2], f[3], ql[j][0], ql[j][1]);
+          if constexpr (PK) {
+            tc::mma<true>((j & 1) ? sacl : sacc, f[0], f[1], f[2], f[3], qh[j][0], qh[j][1]);
+          } else {
+            tc::mma<true>(sacc, f[0], f[1], f[2], f[3], qh[j][0], qh[j][1]);
+            tc::mma<true>(sacl, f[0], f[1], f[2], f[3], ql[j][0], ql[j][1]);
+          }
         }
       } else if constexpr (KS == S_FP8) {  // thread c converts 16-byte chunks 4jj + c of rows g, g+8
 #pragma unroll
@@ -464,8 +502,12 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
             const int j = 4 * jj + e;
             const uint32_t a0 = tc::e4m3x2_f16x2(wa[e] & 0xffffu), a4 = tc::e4m3x2_f16x2(wa[e] >> 16);
             const uint32_t a2 = tc::e4m3x2_f16x2(wb[e] & 0xffffu), a6 = tc::e4m3x2_f16x2(wb[e] >> 16);
-            tc::mma<false>(sacc, a0, a2, a4, a6, qh[j][0], qh[j][1]);
-            tc::mma<false>(sacl, a0, a2, a4, a6, ql[j][0], ql[j][1]);
+            if constexpr (PK) {
+              tc::mma<false>((e & 1) ? sacl : sacc, a0, a2, a4, a6, qh[j][0], qh[j][1]);
+            } else {
+              tc::mma<false>(sacc, a0, a2, a4, a6, qh[j][0], qh[j][1]);
+              tc::mma<false>(sacl, a0, a2, a4, a6, ql[j][0], ql[j][1]);
+            }
           }
         }
       } else {  // group-scaled sides: k-step j is scale group j
@@ -482,7 +524,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
             const uint32_t a0 = tc::e4m3x2_f16x2(wa & 0xffffu), a4 = tc::e4m3x2_f16x2(wa >> 16);
             const uint32_t a2 = tc::e4m3x2_f16x2(wb & 0xffffu), a6 = tc::e4m3x2_f16x2(wb >> 16);
             tc::mma<false>(cg, a0, a2, a4, a6, qh[j][0], qh[j][1]);
-            tc::mma<false>(cg, a0, a2, a4, a6, ql[j][0], ql[j][1]);
+            if constexpr (!PK) tc::mma<false>(cg, a0, a2, a4, a6, ql[j][0], ql[j][1]);
           } else {
             constexpr int B = code_bits(KS);
             const int bit = B * (16 * j + 4 * c);
@@ -504,8 +546,9 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
             const uint2 xa1 = lut_pair(lut_k, pa1, lane);
             const uint2 xb0 = lut_pair(lut_k, pb0, lane);
             const uint2 xb1 = lut_pair(lut_k, pb1, lane);
+            // level hi and lo parts times q (PK: the lo x q-lo term comes along)
             tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, qh[j][0], qh[j][1]);
-            tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
+            if constexpr (!PK) tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
             tc::mma<false>(cg, xa0.y, xb0.y, xa1.y, xb1.y, qh[j][0], qh[j][1]);
           }
           float ga, gb;   // group-j scales of rows g and g+8
@@ -529,6 +572,10 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[e] += sacl[e];
+      if constexpr (PK) {  // q-hi columns + q-lo columns (lanes c, c ^ 2)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(0xffffffffu, sacc[e], 2);
+      }
 
       sout[0] = sacc[0]; sout[1] = sacc[1]; sout[2] = sacc[2]; sout[3] = sacc[3];
   };
@@ -540,11 +587,9 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     // ---- O^T += V^T . P^T
       if constexpr (!VT::GS) {
         // P^T operand (hi + lo) from the accumulator layout
-        uint32_t x1h, x1l, x2h, x2l;
-        tc::split2<VT::BF>(p00, p01, x1h, x1l);
-        tc::split2<VT::BF>(p10, p11, x2h, x2l);
-        const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
-        const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+        uint32_t b[4];
+        p_operand<VT::BF, PK>(p00, p01, p10, p11, c, b);
+        const uint32_t b0h = b[0], b1h = b[1], b0l = b[2], b1l = b[3];
         if constexpr (VS == S_BF16) {
           const int mi = lane >> 3, rr = lane & 7;
           const uint8_t* base = vbh + ((mi >> 1) * 8 + rr) * VT::VRS + (mi & 1) * 16;
@@ -553,7 +598,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
             uint32_t f[4];
             tc::ldsm_x4_t(f, base + i * 32);
             tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0h, b1h);
-            tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0l, b1l);
+            if constexpr (!PK) tc::mma<true>(o[i], f[0], f[1], f[2], f[3], b0l, b1l);
           }
         } else {  // FP8: tokens 2c, 2c+1, 2c+8, 2c+9; dims g*DPT .. g*DPT + DPT - 1
           constexpr int DPT = HD / 8;
@@ -583,7 +628,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
             const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
             const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
             tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
-            tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
+            if constexpr (!PK) tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
           }
         }
       } else if constexpr (VT::CB) {
@@ -592,11 +637,9 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
         // parts, 4-bit scale significand), so P is split once per slab.  Rows
         // g, g+8 of m-tile i are dims 16i + 2g, 16i + 2g + 1; k-slots are
         // tokens 2c, 2c+1, 2c+8, 2c+9.
-        uint32_t x1h, x1l, x2h, x2l;
-        tc::split2<false>(p00, p01, x1h, x1l);
-        tc::split2<false>(p10, p11, x2h, x2l);
-        const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
-        const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+        uint32_t b[4];
+        p_operand<false, PK>(p00, p01, p10, p11, c, b);
+        const uint32_t b0h = b[0], b1h = b[1], b0l = b[2], b1l = b[3];
         const uint8_t* r0 = vbh + (2 * c) * VT::VRS;
         const uint8_t* r1 = vbh + (2 * c + 1) * VT::VRS;
         const uint8_t* r2 = vbh + (2 * c + 8) * VT::VRS;
@@ -633,7 +676,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
           const uint32_t l4_ = tc::hmul2(tc::prmt(e2.y, e3.y, 0x5410u), sc23);
           const uint32_t l6_ = tc::hmul2(tc::prmt(e2.y, e3.y, 0x7632u), sc23);
           tc::mma<false>(o[i], h0, h2, h4, h6, b0h, b1h);
-          tc::mma<false>(o[i], h0, h2, h4, h6, b0l, b1l);
+          if constexpr (!PK) tc::mma<false>(o[i], h0, h2, h4, h6, b0l, b1l);
           tc::mma<false>(o[i], l0_, l2_, l4_, l6_, b0h, b1h);
         }
       } else {
@@ -650,11 +693,9 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
 #pragma unroll
         for (int i = 0; i < NK; ++i) {
           const float ga = tc_group_scale<VS>(vsa, i), gb = tc_group_scale<VS>(vsb, i);
-          uint32_t x1h, x1l, x2h, x2l;
-          tc::split2<false>(p00 * ga, p01 * ga, x1h, x1l);
-          tc::split2<false>(p10 * gb, p11 * gb, x2h, x2l);
-          const uint32_t b0h = tc::movm_t(x1h), b1h = tc::movm_t(x2h);
-          const uint32_t b0l = tc::movm_t(x1l), b1l = tc::movm_t(x2l);
+          uint32_t b[4];
+          p_operand<false, PK>(p00 * ga, p01 * ga, p10 * gb, p11 * gb, c, b);
+          const uint32_t b0h = b[0], b1h = b[1], b0l = b[2], b1l = b[3];
           {
             const int off = 16 * i + 2 * g;
             const uint32_t u0 = *reinterpret_cast<const uint16_t*>(r0 + off);
@@ -666,7 +707,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
             const uint32_t a0 = tc::e4m3x2_f16x2(x01 & 0xffffu), a2 = tc::e4m3x2_f16x2(x01 >> 16);
             const uint32_t a4 = tc::e4m3x2_f16x2(x23 & 0xffffu), a6 = tc::e4m3x2_f16x2(x23 >> 16);
             tc::mma<false>(o[i], a0, a2, a4, a6, b0h, b1h);
-            tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
+            if constexpr (!PK) tc::mma<false>(o[i], a0, a2, a4, a6, b0l, b1l);
           }
         }
       }
@@ -760,18 +801,27 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
     l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
   }
+  if constexpr (PK) {  // P-hi columns + P-lo columns (lanes c, c ^ 2)
+#pragma unroll
+    for (int i = 0; i < NK; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[i][e] += __shfl_xor_sync(0xffffffffu, o[i][e], 2);
+  }
+  const bool writer = !PK || c < 2;
   __syncthreads();  // every warp is done with its ring
   float* mo = reinterpret_cast<float*>(rings);   // [NW warps][8 heads][HD]
   float* ml = mo + NW * 8 * HD;                  // [NW warps][8 heads][m, l]
+  if (writer) {
 #pragma unroll
-  for (int i = 0; i < NK; ++i) {
-    const int da = v_row_dim<VS, HD>(i, g), db = v_row_dim<VS, HD>(i, g + 8);
-    mo[(warp * 8 + 2 * c) * HD + da] = o[i][0];
-    mo[(warp * 8 + 2 * c + 1) * HD + da] = o[i][1];
-    mo[(warp * 8 + 2 * c) * HD + db] = o[i][2];
-    mo[(warp * 8 + 2 * c + 1) * HD + db] = o[i][3];
+    for (int i = 0; i < NK; ++i) {
+      const int da = v_row_dim<VS, HD>(i, g), db = v_row_dim<VS, HD>(i, g + 8);
+      mo[(warp * 8 + 2 * c) * HD + da] = o[i][0];
+      mo[(warp * 8 + 2 * c + 1) * HD + da] = o[i][1];
+      mo[(warp * 8 + 2 * c) * HD + db] = o[i][2];
+      mo[(warp * 8 + 2 * c + 1) * HD + db] = o[i][3];
+    }
   }
-  if (g == 0) {
+  if (g == 0 && writer) {
     ml[(warp * 8 + 2 * c) * 2] = m0;
     ml[(warp * 8 + 2 * c) * 2 + 1] = l0;
     ml[(warp * 8 + 2 * c + 1) * 2] = m1;
@@ -801,11 +851,11 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   }
 }
 
-template <int KS, int VS, int HD>
-cudaError_t launch_tc_inst(const DecodeArgs& a, const Codebooks& cb, cudaStream_t st) {
+template <int KS, int VS, int HD, bool PK>
+cudaError_t launch_tc_kern(const DecodeArgs& a, const Codebooks& cb, cudaStream_t st) {
   using C = TcCfg<KS, VS, HD>;
   static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
-  auto kern = decode_tc_kernel<KS, VS, HD>;
+  auto kern = decode_tc_kernel<KS, VS, HD, PK>;
   if (C::SMEM > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
@@ -813,6 +863,14 @@ cudaError_t launch_tc_inst(const DecodeArgs& a, const Codebooks& cb, cudaStream_
   dim3 grid(a.nsplit, a.nkv, a.num_seqs);
   kern<<<grid, 32 * C::NW, C::SMEM, st>>>(a, cb);
   return cudaGetLastError();
+}
+
+// Up to 4 query heads per KV head leave half of the MMA columns free: they
+// carry the lo parts of q and P (packed instances).
+template <int KS, int VS, int HD>
+cudaError_t launch_tc_inst(const DecodeArgs& a, const Codebooks& cb, cudaStream_t st) {
+  return a.rep <= 4 ? launch_tc_kern<KS, VS, HD, true>(a, cb, st)
+                    : launch_tc_kern<KS, VS, HD, false>(a, cb, st);
 }
 
 template <int KS, int VS>

@@ -19,8 +19,11 @@ LENS = [37, 50, 1, 0, 16, 300, 129]
 
 
 @pytest.mark.parametrize("fmt", ALL_FORMATS)
-@pytest.mark.parametrize("hd,nq,nkv", [(64, 4, 2), (128, 8, 2), (128, 32, 8), (256, 4, 2)])
+@pytest.mark.parametrize("hd,nq,nkv", [(64, 4, 2), (128, 8, 2), (128, 32, 8), (256, 4, 2),
+                                       (64, 16, 2), (128, 16, 2), (256, 16, 2)])
 def test_decode_parity(fmt, hd, nq, nkv):
+    """GQA 2 and 4 run the packed instances (q / P lo parts in the free MMA
+    columns), GQA 8 the unpacked ones."""
     c = decode_case(fmt, LENS, nq, nkv, hd, seed=hd + nq)
     got = gpu_decode(c)
     ref = oracle_decode(c)
