@@ -4,7 +4,7 @@ One step = one decode layer per cache format of the Llama-3-8B-shaped
 workload (32 sequences x 4096 context, 32 query / 8 KV heads, head_dim 128,
 block_size 16; formats bf16, fp8 with a per-tensor scale, turbo4): for each
 format, the cache write of that step's 32 new tokens (one per sequence, at
-position 4095) followed by the split-K paged decode over all 4096 positions.
+position 4095) followed by the paged decode over all 4096 positions.
 The caches (956 MB in total, far above the 129 MB L2) are filled before the
 timed region with the same write kernel.
 
@@ -15,7 +15,7 @@ value  = algorithmic bytes of the step / step time, in GB/s.  Algorithmic
 e2e    = the same bytes / step time measured through the public API with the
          step's inputs copied from pinned host memory and the outputs copied
          back inside the timed region.
-roofline: the dominant kernel (the split-K decode of the bf16 layer, the
+roofline: the dominant kernel (the decode kernel of the format with the
          largest share of the step) against the measured HBM copy bandwidth.
 cpu_baseline: the CPU oracle (numpy) decoding a bounded sample of the same
          workload.
@@ -129,7 +129,7 @@ def algorithmic_decode_bytes(fmt, seq_lens, nkv, hd, bs, window=0):
 
 
 def decode_kernel_name(fmt):
-    """Name of the split-K kernel libkvq launches for this format (label only):
+    """Name of the decode kernel libkvq launches for this format (label only):
     every catalogue format runs on the tensor-core kernel."""
     return "decode_tc_kernel"
 
@@ -341,7 +341,7 @@ def run_gpu(args):
     dom = max(per_layer, key=lambda k: per_layer[k]["us_per_layer"])
     value = step_bytes * ws / (ms_step * 1e-3) / 1e9
     e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
-    launches_per_step = len(fmts) * ((2 if prefill is not None else 1) + 2 * len(windows))
+    launches_per_step = len(fmts) * ((2 if prefill is not None else 1) + len(windows))
     dom_fmt = dom.split("@")[0]
     traffic = TRAFFIC.get((args.workload, dom)) if not args.num_seqs or args.num_seqs == W.make(args.workload).num_seqs else None
     line = {
@@ -355,11 +355,11 @@ def run_gpu(args):
                    "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
         "per_layer": per_layer,
         "cache_write": per_write,
-        "roofline": {"kernel": f"decode_tc_kernel + combine_kernel ({dom})", "bound": "hbm",
+        "roofline": {"kernel": f"decode_tc_kernel ({dom})", "bound": "hbm",
                      "achieved": per_layer[dom]["decode_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": round(per_layer[dom]["decode_gbs"] / peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind + " (hbm_gbs copy)",
-                     "timed": "split + combine kernels per launch, CUDA events on the launch stream"},
+                     "timed": "one decode launch, CUDA events on the launch stream"},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": launches_per_step * args.steps,

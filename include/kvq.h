@@ -186,9 +186,12 @@ kvq_status kvq_cache_write(
 
 /* ------------------------------------------------------------ paged decode */
 
-/* Bytes of fp32 scratch kvq_paged_decode needs for these arguments (split-K
- * partial results); the split count depends on the current device's SM
- * count, so query on the device that will run the decode. 0 on error. */
+/* Bytes of device scratch kvq_paged_decode needs for these arguments: fp32
+ * partial results of (sequence, query head) rows that several CTAs share,
+ * followed by one int32 merge counter per (sequence, kv head) (the last
+ * 16-byte-rounded num_seqs*num_kv_heads*4 bytes).  The size depends on the
+ * current device's SM count, so query on the device that will run the
+ * decode.  0 on error. */
 size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                   int32_t num_kv_heads, int32_t head_dim,
                                   int32_t block_size, int32_t max_blocks_per_seq,
@@ -217,11 +220,19 @@ size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *   sm_scale     logit scale; 0 selects 1/sqrt(head_dim)
  *   k_scale, v_scale  per-tensor FP8 scales (FP8 sides only)
  *   sparse_v_threshold  0 = exact; > 0 drops the V term of a position whose
- *                weight (normalised within its split, which over-estimates
- *                the global weight, so it never drops more) is <= threshold
+ *                weight (normalised by the part of the sequence one warp has
+ *                seen so far, which over-estimates the global weight, so it
+ *                never drops more) is <= threshold
  *   workspace    device, >= kvq_decode_workspace_bytes(...) bytes, 16-byte
- *                aligned; contents on entry are ignored
- *   error_flag   optional device int32 */
+ *                aligned, all zero on entry.  Every call leaves the whole
+ *                workspace zero again, so one zeroed once can be reused by
+ *                any number of calls, of any shapes, in stream order; calls
+ *                that may run at the same time need separate workspaces.
+ *   error_flag   optional device int32
+ *
+ * One kernel launch: persistent CTAs (two per SM) each take an equal share
+ * of all (sequence, kv head) rows' 16-token slabs; rows shared by several
+ * CTAs are merged by the last of them to finish. */
 kvq_status kvq_paged_decode(
     const void* q, kvq_dtype q_dtype, int64_t q_stride,
     const void* k_cache, const void* v_cache,
@@ -250,8 +261,9 @@ kvq_status kvq_paged_decode(
  * synchronization is not acceptable.
  *
  * Same arguments and results as kvq_paged_decode, minus the workspace: the
- * split-K partials go to a fixed KVQ_NOALLOC_SCRATCH_BYTES array compiled
- * into the library.  Nothing is allocated (no cudaMalloc / cudaFree).
+ * partials and merge counters go to a fixed KVQ_NOALLOC_SCRATCH_BYTES array
+ * compiled into the library (zero when the library loads; every call leaves
+ * it zero).  Nothing is allocated (no cudaMalloc / cudaFree).
  *   - Returns KVQ_ERR_WORKSPACE if kvq_decode_workspace_bytes(...) for these
  *     arguments exceeds KVQ_NOALLOC_SCRATCH_BYTES.
  *   - The first call with a given device current looks the array's device

@@ -139,40 +139,39 @@ int sm_count() {
   return n;
 }
 
-struct SplitPlan {
-  int nsplit;
-  int pages_per_split;
+// Decode partition.  The decode runs persistent CTAs, two per SM, each on an
+// equal share of all (sequence, kv head) units' 16-token slabs, at least
+// min_slabs of them (measured on GB300: one balanced wave of long CTAs beats
+// more, shorter split CTAs, which pay the prologue and merge more often and
+// leave a partial last wave).  kmax bounds the partials of one unit: a unit
+// of n slabs spans at most floor((n - 1) / per_cta) + 2 CTAs, and per_cta >=
+// max(min_slabs, num_kv_heads * n / grid) because every kv head of a
+// sequence is a unit of the same length.
+struct DecodePlan {
+  int grid, min_slabs, kmax;
 };
 
-// Flash-decoding split: enough CTAs of (split, kv head, sequence) to fill the
-// SMs several times, each split at least two 32-token tiles long.
-// ctas_per_sm = 3 (measured on GB300: long splits amortize the decode
-// kernel's prologue and merge).
-SplitPlan plan_split(int num_seqs, int nkv, int bs, int max_blocks, int window, int sms,
-                     int ctas_per_sm) {
-  const int tp = 32 / bs;
-  int pages = max_blocks;
-  if (window > 0) {
-    const int wp = (window + bs - 1) / bs + 1;
-    if (wp < pages) pages = wp;
-  }
-  if (pages < 1) pages = 1;
-  const int64_t units = (int64_t)num_seqs * nkv;
-  const int64_t target = (int64_t)(sms > 0 ? sms : 148) * ctas_per_sm;
-  int64_t ns = units > 0 ? (target + units - 1) / units : 1;
-  const int64_t max_ns = std::max<int64_t>(1, pages / (2 * tp));
-  ns = std::min(std::max<int64_t>(ns, 1), max_ns);
-  int pps = (int)((pages + ns - 1) / ns);
-  pps = (pps + tp - 1) / tp * tp;
-  if (pps > 512) pps = 512;  // the tensor-core kernel stages a split's block ids in smem
-  const int nsplit = (pages + pps - 1) / pps;
-  return {nsplit, pps};
+DecodePlan plan_decode(int nkv, int bs, int max_blocks, int window, int sms) {
+  DecodePlan p{};
+  p.grid = 2 * (sms > 0 ? sms : 148);
+  p.min_slabs = 16;
+  int64_t max_n = ((int64_t)max_blocks * bs + 15) / 16;
+  if (window > 0) max_n = std::min<int64_t>(max_n, (window + 15) / 16 + 1);
+  if (max_n < 1) max_n = 1;
+  const int64_t by_len = (max_n - 1) / p.min_slabs + 2;
+  const int64_t by_grid = (p.grid + nkv - 1) / nkv + 1;
+  p.kmax = (int)std::min(by_len, by_grid);
+  return p;
 }
 
-#ifndef KVQ_SPLIT_CTAS_PER_SM
-#define KVQ_SPLIT_CTAS_PER_SM 3
-#endif
-int split_ctas_per_sm(kvq_format) { return KVQ_SPLIT_CTAS_PER_SM; }
+// Workspace: partials [num_seqs][nq][kmax][hd + 4] fp32, then the partial
+// counts [num_seqs][nkv] int32.
+size_t part_bytes(int num_seqs, int nq, int hd, const DecodePlan& p) {
+  return (size_t)num_seqs * nq * p.kmax * (hd + 4) * sizeof(float);
+}
+size_t workspace_need(int num_seqs, int nq, int nkv, int hd, const DecodePlan& p) {
+  return part_bytes(num_seqs, nq, hd, p) + ((size_t)num_seqs * nkv * sizeof(int32_t) + 15) / 16 * 16;
+}
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -326,9 +325,7 @@ size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t nq, int32_t nkv, int
   if (!fmt_ok(fmt) || num_seqs < 0 || nq < 1 || nkv < 1 || hd < 1 || bs < 1 || max_blocks < 1 ||
       window < 0 || (bs != 8 && bs != 16 && bs != 32))
     return 0;
-  const SplitPlan p = plan_split(num_seqs, nkv, bs, max_blocks, window, sm_count(),
-                                 split_ctas_per_sm(fmt));
-  return (size_t)num_seqs * nq * p.nsplit * (hd + 4) * sizeof(float);
+  return workspace_need(num_seqs, nq, nkv, hd, plan_decode(nkv, bs, max_blocks, window, sm_count()));
 }
 
 kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, const void* k_cache,
@@ -367,9 +364,8 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   if ((ks == S_FP8 && !(k_scale > 0.f && std::isfinite(k_scale))) ||
       (vs == S_FP8 && !(v_scale > 0.f && std::isfinite(v_scale))))
     return fail(KVQ_ERR_ARG, "FP8 side needs a finite scale > 0");
-  const int sms = sm_count();
-  const SplitPlan p = plan_split(num_seqs, nkv, bs, max_blocks, window, sms, split_ctas_per_sm(fmt));
-  const size_t need = (size_t)num_seqs * nq * p.nsplit * (hd + 4) * sizeof(float);
+  const DecodePlan p = plan_decode(nkv, bs, max_blocks, window, sm_count());
+  const size_t need = workspace_need(num_seqs, nq, nkv, hd, p);
   if (workspace_bytes < need)
     return fail(KVQ_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!decode_tc_supported(ks, vs)) return fail(KVQ_ERR_FORMAT, "no decode instance for this pair");
@@ -399,24 +395,17 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   a.inv_sqrt_hd = (float)(1.0 / std::sqrt((double)hd));
   a.window = window;
   a.sparse_thr = sparse_v_threshold;
-  a.pages_per_split = p.pages_per_split;
-  a.nsplit = p.nsplit;
+  a.grid = p.grid;
+  a.min_slabs = p.min_slabs;
+  a.kmax = p.kmax;
   a.part = (float*)workspace;
+  a.counters = (int32_t*)((uint8_t*)workspace + part_bytes(num_seqs, nq, hd, p));
+  a.out = out;
+  a.out_bf16 = out_dtype == KVQ_DTYPE_BF16;
   a.err = error_flag;
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_decode_tc(ks, vs, hd, a, cb, st);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-  CombineArgs c{};
-  c.part = a.part;
-  c.out = out;
-  c.out_bf16 = out_dtype == KVQ_DTYPE_BF16;
-  c.num_seqs = num_seqs;
-  c.nq = nq;
-  c.nsplit = p.nsplit;
-  c.v_rotated = side_rotated(vs) ? 1 : 0;
-  c.inv_sqrt_hd = a.inv_sqrt_hd;
-  e = launch_combine(c, hd, st);
-  if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

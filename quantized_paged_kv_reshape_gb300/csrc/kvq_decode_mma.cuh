@@ -1,31 +1,39 @@
-// Split-K paged decode with the GQA contraction on tensor cores.
+// Paged decode attention on tensor cores, one kernel launch.
 //
-// Same result as decode_split_kernel ("combs_models/kv.rs" attend + repeat_kv
-// for one query over the pages of the block tables; "spark_runtime/
-// kv_cache.rs" is_wht_rotated bookends), for sides whose stored values are
-// exact in a 16-bit MMA operand: BF16 (bf16 operands) and FP8 E4M3 (fp16
-// operands; the per-tensor scale is applied to the fp32 results).
+// Computes "combs_models/kv.rs" attend (scores, softmax, P.V) with
+// repeat_kv for one query per sequence over the pages of its block table,
+// with the "spark_runtime/kv_cache.rs" is_wht_rotated bookends: q is rotated
+// forward when K is stored rotated and the output back when V is.
+//
+// Work split.  The (sequence, kv head) rows, laid end to end in 16-token
+// slabs, are cut into one equal stretch per persistent CTA (two per SM);
+// the NW warps of a CTA take slabs w, w+NW, ... of a stretch, each with a
+// private cp.async ring, and are merged through shared memory.  A row cut by
+// CTA boundaries leaves one partial (m, l, acc) per CTA in the workspace;
+// the last CTA to finish the row merges them (online-softmax identity),
+// normalises, rotates back and stores the output.
 //
 // Per warp and per slab of 16 token positions:
-//   S^T[16 tok x 8 q-heads] = K[16 x hd] . Q^T[hd x 8]      (m16n8k16, hd/16 steps)
+//   S^T[16 tok x 8 cols] = K[16 x hd] . Q^T[hd x 8]      (m16n8k16, hd/16 steps)
 //   online softmax on the fp32 accumulators (exp2 domain)
-//   O^T[hd x 8] += V^T[hd x 16 tok] . P^T[16 x 8]           (hd/16 m-tiles)
-// The query and P operands are split into hi + lo 16-bit parts (two MMAs
-// each), so the products carry ~16 significant bits: a single 16-bit pass
-// misses the 2e-3 output bound on outlier-heavy inputs.  K and V values are
-// exact in the operand type, so they need no split.  P^T's operand
-// fragments come from the S accumulators by an in-register 8x8 transpose
-// (movmatrix).  BF16 rows go to the MMAs through ldmatrix (.trans for V);
-// FP8 rows are converted in registers: K's reduction dimension is permuted
-// per thread so that each thread converts whole 16-byte chunks (q uses the
-// same permutation), and V's E4M3 bytes of two tokens are byte-interleaved
-// (prmt) before the e4m3x2 -> f16x2 conversion, with the output dims of the
-// fragments permuted accordingly.
-//
-// Each warp owns a private cp.async ring of slabs (no CTA barrier inside the
-// loop); the NW warps of a CTA take slabs w, w+NW, ... of the split and are
-// merged through shared memory at the end.  Positions outside [lo, L), past
-// the split or with a bad block id are zero-filled and masked to -inf.
+//   O^T[hd x 8] += V^T[hd x 16 tok] . P^T[16 x 8]        (hd/16 m-tiles)
+// The query and P operands are split into hi + lo 16-bit parts, so the
+// products carry ~16 significant bits: a single 16-bit pass misses the 2e-3
+// output bound on outlier-heavy inputs.  With at most 4 query heads per kv
+// head the lo parts ride in the otherwise idle columns 4-7 and are added to
+// columns 0-3 by one shuffle; with more, they take a second MMA.  P^T's
+// operand fragments come from the S accumulators by an in-register 8x8
+// transpose (movmatrix).
+// Operands by side: BF16 rows through ldmatrix (.trans for V); FP8 E4M3
+// converted in registers (K's reduction dimension permuted per thread so
+// that each thread converts whole 16-byte chunks, V's bytes of two tokens
+// interleaved with prmt); Turbo2/3/4 codes through a shared-memory LUT of
+// code pairs whose levels are split into two 7-bit parts, exact in fp16 when
+// multiplied by an E4M3 group scale (K: scale applied per 16-dim k-step to
+// the fp32 products; V: folded into the operand); Turbo8 E4M3 data with its
+// BF16 group scale applied to the products (K) or to P (V).
+// Positions outside the attended range or with a bad block id are
+// zero-filled and masked to -inf.
 #pragma once
 
 #include <math_constants.h>
@@ -187,10 +195,11 @@ struct TcCfg {
   static constexpr int STAGE = (OFF_VS + SLAB * V::SROW + 15) / 16 * 16;
   static constexpr bool SHARE_LUT = K::CB && V::CB && code_bits(KS) == code_bits(VS);
   static constexpr int LUTS = K::LUT_BYTES + (SHARE_LUT ? 0 : V::LUT_BYTES);
-  static constexpr int MAXP = 512;                             // pages per split (host cap)
+  static constexpr int MAXP = 512;                             // pages staged per stretch
   static constexpr int OFF_BLK = 8 * HD * 4;                   // after q_s [8][HD] fp32
-  static constexpr int OFF_OFFS = OFF_BLK + MAXP * 4;          // int32 block ids of the split
-  static constexpr int OFF_LUT = OFF_OFFS + NW * 128 * 8;      // per-warp row offsets
+  static constexpr int OFF_OFFS = OFF_BLK + MAXP * 4;          // int32 block ids of a stretch
+  static constexpr int OFF_SCAN = OFF_OFFS + NW * 128 * 8;     // per-warp row offsets
+  static constexpr int OFF_LUT = OFF_SCAN + 16 * 8;            // partition scan scratch
   static constexpr int OFF_RING = OFF_LUT + LUTS;
   static constexpr int BUDGET = 112 * 1024 - OFF_RING;         // two CTAs per SM
   static constexpr int NST0 = BUDGET / (NW * STAGE);
@@ -309,49 +318,104 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int split = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
-  const int bs = a.bs;
-  const int L = a.seq_lens[seq];
-  const int lo = a.window > 0 ? max(0, L - a.window) : 0;
-  const int first_page = lo / bs;
-  int end_page = (L + bs - 1) / bs;
-  if (end_page > a.max_blocks) {
-    if (tid == 0 && split == 0 && a.err) atomicOr(a.err, 2);
-    end_page = a.max_blocks;
-  }
-  const int p0 = first_page + split * a.pages_per_split;
-  const int p1 = min(min(p0 + a.pages_per_split, end_page), p0 + C::MAXP);
-  const size_t pstride = (size_t)a.nsplit * (HD + 4);
-  float* part = a.part + ((size_t)(seq * a.nq + kvh * a.rep) * a.nsplit + split) * (HD + 4);
-  if (p0 >= p1) {
-    for (int j = warp; j < a.rep; j += NW)
-      for (int i = lane; i < HD + 4; i += 32) part[j * pstride + i] = (i == 0) ? -CUDART_INF_F : 0.f;
-    return;
-  }
-
-  const int tok0 = p0 * bs;
-  const int tok_end = min(p1 * bs, L);
   constexpr int SLAB = C::SLAB;
-  const int nslab = (tok_end - tok0 + SLAB - 1) / SLAB;
-  const int my = nslab > warp ? (nslab - 1 - warp) / NW + 1 : 0;
-  const int64_t tab = (int64_t)seq * a.max_blocks;
+  const int bs = a.bs;
+  const int lbs = 31 - __clz(bs);  // block_size is a power of two
+  const int nkv = a.nkv;
+  const int64_t cap = (int64_t)a.max_blocks * bs;  // positions the block table covers
   uint8_t* ring = rings + warp * C::NST * C::STAGE;
   int* blk_s = reinterpret_cast<int*>(smem + C::OFF_BLK);
   int64_t* offs = reinterpret_cast<int64_t*>(smem + C::OFF_OFFS) + warp * 128;
-  const int lbs = 31 - __clz(bs);  // block_size is a power of two
+  int64_t* scan_s = reinterpret_cast<int64_t*>(smem + C::OFF_SCAN);
 
-  // Block ids of the split's pages, staged once (-1 = outside the pool).
-  for (int i = tid; i < p1 - p0; i += NT) {
-    const int64_t b = a.block_tables[tab + p0 + i];
-    const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
-    if (bad && a.err) atomicOr(a.err, 2);
-    blk_s[i] = bad ? -1 : (int)b;
+  // Attended positions [lo, len) of sequence s and the 16-token slabs
+  // [first, first + n) that hold them.
+  auto seq_slabs = [&](int s, int& first, int& n, int& lo_, int& len) {
+    len = a.seq_lens[s];
+    if (len > cap) len = (int)cap;
+    if (len <= 0) {
+      first = n = lo_ = len = 0;
+      return;
+    }
+    lo_ = a.window > 0 ? max(0, len - a.window) : 0;
+    first = lo_ >> 4;
+    n = ((len + 15) >> 4) - first;
+  };
+
+  // ---- Partition.  The (sequence, kv head) units, sequence-major, are laid
+  // end to end in slabs (T in all); CTA b takes slabs [b * cpc, (b + 1) *
+  // cpc), cpc = max(ceil(T / gridDim), min_slabs), so every CTA gets the same
+  // amount of work whatever the lengths.  A unit cut by CTA boundaries leaves
+  // one partial per CTA, in slot (CTA - first CTA of the unit).
+  const int N = a.num_seqs;
+  const int chunk = (N + NT - 1) / NT;
+  const int s_beg = min(N, tid * chunk), s_end = min(N, s_beg + chunk);
+  int64_t mine = 0;
+  for (int s = s_beg; s < s_end; ++s) {
+    int f, n, l_, e_;
+    seq_slabs(s, f, n, l_, e_);
+    mine += n;
+    if (blockIdx.x == 0 && a.seq_lens[s] > cap && a.err) atomicOr(a.err, 2);
   }
+  int64_t incl = mine;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) scan_s[warp] = incl;
+  __syncthreads();
+  int64_t before = 0, total = 0;
+  for (int w2 = 0; w2 < NW; ++w2) {
+    const int64_t v = scan_s[w2];
+    if (w2 < warp) before += v;
+    total += v;
+  }
+  const int64_t excl = before + incl - mine;  // slabs of one kv head before this chunk
+  const int64_t T = total * nkv;
+  int64_t cpc = (T + gridDim.x - 1) / gridDim.x;
+  if (cpc < a.min_slabs) cpc = a.min_slabs;
+  const int64_t x0 = (int64_t)blockIdx.x * cpc;
+  const int64_t x_end = min(x0 + cpc, T);
+  __syncthreads();  // scan_s is reused below
+  if (blockIdx.x == 0) {  // sequences with nothing to attend get zero rows
+    for (int s = s_beg; s < s_end; ++s) {
+      int f, n, l_, e_;
+      seq_slabs(s, f, n, l_, e_);
+      if (n > 0) continue;
+      for (int i = 0; i < a.nq * HD; ++i) {
+        const int64_t o_ = (int64_t)s * a.nq * HD + i;
+        if (a.out_bf16) reinterpret_cast<uint16_t*>(a.out)[o_] = 0;
+        else reinterpret_cast<float*>(a.out)[o_] = 0.f;
+      }
+    }
+  }
+  if (x0 < T && nkv * excl <= x0 && x0 < nkv * (excl + mine)) {  // the chunk holding x0
+    int64_t P = excl;
+    for (int s = s_beg; s < s_end; ++s) {
+      int f, n, l_, e_;
+      seq_slabs(s, f, n, l_, e_);
+      if (x0 < nkv * (P + n)) {
+        const int64_t r = x0 - nkv * P;
+        scan_s[0] = s;
+        scan_s[1] = r / n;
+        scan_s[2] = r % n;
+        break;
+      }
+      P += n;
+    }
+  }
+  __syncthreads();
+  if (x0 >= T) return;
+  int seq = (int)scan_s[0], kvh = (int)scan_s[1];
+  int64_t off = scan_s[2];
+
   // Pair LUTs of the codebook sides: entry p = (code of dim 2k) | (code of
   // dim 2k+1) << b holds fp16 (hi, hi) and (lo, lo) where hi and lo carry 7
   // significant bits each and level = hi + lo to ~2^-16 relative.  With 7
   // bits, hi and lo times an E4M3 group scale (4 significant bits) are exact
-  // in fp16, which lets the V operand absorb its group scale.
+  // in fp16, which lets the V operand absorb its group scale.  Filled once
+  // per CTA.
   auto fill_lut = [&](uint2* lut, const float* lv, int bits) {
     const int n = 1 << bits;
     for (int e = tid; e < n * n * 16; e += NT) {
@@ -367,7 +431,11 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   if constexpr (VT::CB && !C::SHARE_LUT)
     fill_lut(reinterpret_cast<uint2*>(smem + C::OFF_LUT + KT::LUT_BYTES), side_levels<VS>(cb),
              code_bits(VS));
-  __syncthreads();
+
+  // State of the current stretch: attended positions [lo, tok_end), slabs
+  // from tok0, block ids of pages p0 .. staged in blk_s.
+  int lo = 0, tok_end = 0, tok0 = 0, p0 = 0;
+  int64_t tab = 0;
 
   // Block id of position pos, or -1 if it is not attended / not valid.
   auto pos_block = [&](int pos) -> int {
@@ -388,9 +456,9 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       const int q = lane + 32 * k;
       if (TOT % 32 == 0 || q < TOT) {
         const int row = q / NC, ch = q - row * NC;
-        const int64_t off = tbl[row];
-        const bool ok = off >= 0;
-        cp_async<CHB>(dst + row * dst_stride + ch * CHB, base + (ok ? off : 0) + ch * CHB, ok);
+        const int64_t o_ = tbl[row];
+        const bool ok = o_ >= 0;
+        cp_async<CHB>(dst + row * dst_stride + ch * CHB, base + (ok ? o_ : 0) + ch * CHB, ok);
       }
     }
   };
@@ -399,7 +467,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     uint8_t* sb = ring + (s % C::NST) * C::STAGE;
     const int slab_pos = tok0 + (warp + NW * s) * SLAB;
     const int b = pos_block(slab_pos + lane);
-    const int64_t rr = (int64_t)((slab_pos + lane) & (bs - 1)) * a.nkv + kvh;   // row in block
+    const int64_t rr = (int64_t)((slab_pos + lane) & (bs - 1)) * nkv + kvh;   // row in block
     const int64_t bk = (int64_t)b * a.k_bstride, bv = (int64_t)b * a.v_bstride;
     if (lane < SLAB) {
       offs[lane] = b < 0 ? -1 : bk + rr * KT::ROW;
@@ -420,55 +488,12 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
                 std::integral_constant<int, VT::SROW>{}, std::integral_constant<int, VT::SCH>{});
   };
 
-#pragma unroll
-  for (int s = 0; s < C::NST - 1; ++s) {
-    if (s < my) issue(s);
-    cp_async_commit();
-  }
-
-  // ---- queries (rotated when K is stored rotated), rows >= rep are zero
-  for (int j = warp; j < 8; j += NW) {
-    float x[E];
-    if (j < a.rep) {
-      const int64_t qoff = (int64_t)seq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
-#pragma unroll
-      for (int i = 0; i < E; ++i)
-        x[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
-                        : reinterpret_cast<const float*>(a.q)[qoff + i];
-      if constexpr (side_rotated(KS)) fwht_warp<E>(x, lane, a.inv_sqrt_hd);
-    } else {
-#pragma unroll
-      for (int i = 0; i < E; ++i) x[i] = 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < E; ++i) q_s[j * HD + lane * E + i] = x[i];
-  }
-  __syncthreads();  // q_s complete (copies of the first slabs are in flight)
   // Q^T operand (B column n = g).  PK: column g carries head g & 3, its hi
   // part for g < 4 and its lo part for g >= 4 (qh only); otherwise column g
   // is head g, with the hi and lo parts in separate operands qh, ql.
   uint32_t qh[NK][2], ql[PK ? 1 : NK][2];
-#pragma unroll
-  for (int j = 0; j < NK; ++j) {
-    int d[4];
-    k_slot_dims<KS, HD>(j, c, d);
-    const float* qr = q_s + (PK ? (g & 3) : g) * HD;
-    uint32_t h0, l0, h1, l1;
-    tc::split2<KT::BF>(qr[d[0]], qr[d[1]], h0, l0);
-    tc::split2<KT::BF>(qr[d[2]], qr[d[3]], h1, l1);
-    if constexpr (PK) {
-      qh[j][0] = g < 4 ? h0 : l0;
-      qh[j][1] = g < 4 ? h1 : l1;
-    } else {
-      qh[j][0] = h0; ql[j][0] = l0;
-      qh[j][1] = h1; ql[j][1] = l1;
-    }
-  }
-
   float o[NK][4];
-#pragma unroll
-  for (int i = 0; i < NK; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  float m0, m1, l0, l1;
   const float scale = a.score_scale;
 
   // S^T of the 16 positions whose K rows start at kbh (scale rows at ksbh).
@@ -713,140 +738,302 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       }
   };
 
-  for (int s = 0; s < my; ++s) {
-    cp_async_wait<C::NST - 2>();
-    __syncwarp();
-    if (s + C::NST - 1 < my) issue(s + C::NST - 1);
-    cp_async_commit();
-    const uint8_t* sb = ring + (s % C::NST) * C::STAGE;
-    const int slab_pos = tok0 + (warp + NW * s) * SLAB;
 
-    // ---- scores of both row tiles; this thread holds rows g, g+8 of each
-    constexpr int NH = C::NH;
-    float sv[2][4] = {{-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F},
-                      {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F}};
+  // ---- the units of this CTA's slab range
+  int64_t x = x0;
+  while (x < x_end && seq < N) {
+    int first, n, len;
+    seq_slabs(seq, first, n, lo, len);
+    const int64_t take = min((int64_t)n - off, x_end - x);
+    const int64_t ou = x - off;                            // the unit's first slab
+    const int slot = (int)(blockIdx.x - ou / cpc);         // this CTA's partial
+    const int np = (int)((ou + n - 1) / cpc - ou / cpc + 1);  // CTAs on the unit
+    tab = (int64_t)seq * a.max_blocks;
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      float sc4[4];
-      scores16(sb + 16 * h * KT::KRS, sb + C::OFF_KS + 16 * h * KT::SROW, sc4);
-      const bool va = pos_block(slab_pos + 16 * h + g) >= 0;
-      const bool vb_ = pos_block(slab_pos + 16 * h + g + 8) >= 0;
-      sv[h][0] = va ? sc4[0] * scale : -CUDART_INF_F;
-      sv[h][1] = va ? sc4[1] * scale : -CUDART_INF_F;
-      sv[h][2] = vb_ ? sc4[2] * scale : -CUDART_INF_F;
-      sv[h][3] = vb_ ? sc4[3] * scale : -CUDART_INF_F;
+    for (int i = 0; i < NK; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    m0 = m1 = -CUDART_INF_F;
+    l0 = l1 = 0.f;
+    // Stretches of at most MAXP pages (the staged block ids).
+    const int sub = (C::MAXP - 1) * bs / SLAB;
+    const int64_t s_lo = first + off, s_hi = first + off + take;
+    for (int64_t sa = s_lo; sa < s_hi; sa += sub) {
+      const int nsl = (int)min((int64_t)sub, s_hi - sa);
+      tok0 = (int)(sa * SLAB);
+      tok_end = min(tok0 + nsl * SLAB, len);
+      p0 = tok0 >> lbs;
+      const int p1 = ((tok_end - 1) >> lbs) + 1;
+      __syncthreads();  // blk_s, q_s and the rings are free
+      if (sa == s_lo) {
+        // ---- queries (rotated when K is stored rotated), rows >= rep are zero
+        for (int j = warp; j < 8; j += NW) {
+          float xq[E];
+          if (j < a.rep) {
+            const int64_t qoff = (int64_t)seq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
+#pragma unroll
+            for (int i = 0; i < E; ++i)
+              xq[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
+                               : reinterpret_cast<const float*>(a.q)[qoff + i];
+            if constexpr (side_rotated(KS)) fwht_warp<E>(xq, lane, a.inv_sqrt_hd);
+          } else {
+#pragma unroll
+            for (int i = 0; i < E; ++i) xq[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < E; ++i) q_s[j * HD + lane * E + i] = xq[i];
+        }
+      }
+      // Block ids of the stretch's pages (-1 = outside the pool).
+      for (int i = tid; i < p1 - p0; i += NT) {
+        const int64_t b = a.block_tables[tab + p0 + i];
+        const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
+        if (bad && a.err) atomicOr(a.err, 2);
+        blk_s[i] = bad ? -1 : (int)b;
+      }
+      __syncthreads();
+      const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
+#pragma unroll
+      for (int s = 0; s < C::NST - 1; ++s) {
+        if (s < my) issue(s);
+        cp_async_commit();
+      }
+      if (sa == s_lo) {
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+          int d[4];
+          k_slot_dims<KS, HD>(j, c, d);
+          const float* qr = q_s + (PK ? (g & 3) : g) * HD;
+          uint32_t h0, lq0, h1, lq1;
+          tc::split2<KT::BF>(qr[d[0]], qr[d[1]], h0, lq0);
+          tc::split2<KT::BF>(qr[d[2]], qr[d[3]], h1, lq1);
+          if constexpr (PK) {
+            qh[j][0] = g < 4 ? h0 : lq0;
+            qh[j][1] = g < 4 ? h1 : lq1;
+          } else {
+            qh[j][0] = h0; ql[j][0] = lq0;
+            qh[j][1] = h1; ql[j][1] = lq1;
+          }
+        }
+      }
+      for (int s = 0; s < my; ++s) {
+        cp_async_wait<C::NST - 2>();
+        __syncwarp();
+        if (s + C::NST - 1 < my) issue(s + C::NST - 1);
+        cp_async_commit();
+        const uint8_t* sb = ring + (s % C::NST) * C::STAGE;
+        const int slab_pos = tok0 + (warp + NW * s) * SLAB;
+
+        // ---- scores of both row tiles; this thread holds rows g, g+8 of each
+        constexpr int NH = C::NH;
+        float sv[2][4] = {{-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F},
+                          {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F}};
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          float sc4[4];
+          scores16(sb + 16 * h * KT::KRS, sb + C::OFF_KS + 16 * h * KT::SROW, sc4);
+          const bool va = pos_block(slab_pos + 16 * h + g) >= 0;
+          const bool vb_ = pos_block(slab_pos + 16 * h + g + 8) >= 0;
+          sv[h][0] = va ? sc4[0] * scale : -CUDART_INF_F;
+          sv[h][1] = va ? sc4[1] * scale : -CUDART_INF_F;
+          sv[h][2] = vb_ ? sc4[2] * scale : -CUDART_INF_F;
+          sv[h][3] = vb_ ? sc4[3] * scale : -CUDART_INF_F;
+        }
+
+        // ---- online softmax over the slab's positions (cols 2c, 2c+1)
+        float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2]));
+        float mx1 = fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]));
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, msk));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, msk));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        float al0 = 1.f, al1 = 1.f;
+        float pw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        if (mn0 != -CUDART_INF_F) {
+          al0 = exp2f(m0 - mn0);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            pw[h][0] = exp2f(sv[h][0] - mn0);
+            pw[h][2] = exp2f(sv[h][2] - mn0);
+          }
+        }
+        if (mn1 != -CUDART_INF_F) {
+          al1 = exp2f(m1 - mn1);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            pw[h][1] = exp2f(sv[h][1] - mn1);
+            pw[h][3] = exp2f(sv[h][3] - mn1);
+          }
+        }
+        l0 = l0 * al0 + (pw[0][0] + pw[0][2]) + (pw[1][0] + pw[1][2]);
+        l1 = l1 * al1 + (pw[0][1] + pw[0][3]) + (pw[1][1] + pw[1][3]);
+        m0 = mn0;
+        m1 = mn1;
+        if (a.sparse_thr > 0.f) {  // drop weights <= thr x (this warp's running sum)
+          float t0 = l0, t1 = l1;
+#pragma unroll
+          for (int msk = 4; msk < 32; msk <<= 1) {
+            t0 += __shfl_xor_sync(0xffffffffu, t0, msk);
+            t1 += __shfl_xor_sync(0xffffffffu, t1, msk);
+          }
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            if (pw[h][0] <= a.sparse_thr * t0) pw[h][0] = 0.f;
+            if (pw[h][2] <= a.sparse_thr * t0) pw[h][2] = 0.f;
+            if (pw[h][1] <= a.sparse_thr * t1) pw[h][1] = 0.f;
+            if (pw[h][3] <= a.sparse_thr * t1) pw[h][3] = 0.f;
+          }
+        }
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int i = 0; i < NK; ++i) {
+            o[i][0] *= al0; o[i][1] *= al1; o[i][2] *= al0; o[i][3] *= al1;
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          pv16(sb + C::OFF_V + 16 * h * VT::VRS, sb + C::OFF_VS + 16 * h * VT::SROW, pw[h][0],
+               pw[h][1], pw[h][2], pw[h][3]);
+      }
+      cp_async_wait<0>();
     }
 
-    // ---- online softmax over the slab's positions (cols 2c, 2c+1)
-    float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2]));
-    float mx1 = fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]));
 #pragma unroll
     for (int msk = 4; msk < 32; msk <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, msk));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, msk));
+      l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    float al0 = 1.f, al1 = 1.f;
-    float pw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if (mn0 != -CUDART_INF_F) {
-      al0 = exp2f(m0 - mn0);
+    if constexpr (PK) {  // P-hi columns + P-lo columns (lanes c, c ^ 2)
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        pw[h][0] = exp2f(sv[h][0] - mn0);
-        pw[h][2] = exp2f(sv[h][2] - mn0);
-      }
+      for (int i = 0; i < NK; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[i][e] += __shfl_xor_sync(0xffffffffu, o[i][e], 2);
     }
-    if (mn1 != -CUDART_INF_F) {
-      al1 = exp2f(m1 - mn1);
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        pw[h][1] = exp2f(sv[h][1] - mn1);
-        pw[h][3] = exp2f(sv[h][3] - mn1);
-      }
-    }
-    l0 = l0 * al0 + (pw[0][0] + pw[0][2]) + (pw[1][0] + pw[1][2]);
-    l1 = l1 * al1 + (pw[0][1] + pw[0][3]) + (pw[1][1] + pw[1][3]);
-    m0 = mn0;
-    m1 = mn1;
-    if (a.sparse_thr > 0.f) {  // drop weights <= thr x (this warp's running sum)
-      float t0 = l0, t1 = l1;
-#pragma unroll
-      for (int msk = 4; msk < 32; msk <<= 1) {
-        t0 += __shfl_xor_sync(0xffffffffu, t0, msk);
-        t1 += __shfl_xor_sync(0xffffffffu, t1, msk);
-      }
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        if (pw[h][0] <= a.sparse_thr * t0) pw[h][0] = 0.f;
-        if (pw[h][2] <= a.sparse_thr * t0) pw[h][2] = 0.f;
-        if (pw[h][1] <= a.sparse_thr * t1) pw[h][1] = 0.f;
-        if (pw[h][3] <= a.sparse_thr * t1) pw[h][3] = 0.f;
-      }
-    }
-    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+    const bool writer = !PK || c < 2;
+    __syncthreads();  // every warp is done with its ring
+    float* mo = reinterpret_cast<float*>(rings);   // [NW warps][8 heads][HD]
+    float* ml = mo + NW * 8 * HD;                  // [NW warps][8 heads][m, l]
+    if (writer) {
 #pragma unroll
       for (int i = 0; i < NK; ++i) {
-        o[i][0] *= al0; o[i][1] *= al1; o[i][2] *= al0; o[i][3] *= al1;
+        const int da = v_row_dim<VS, HD>(i, g), db = v_row_dim<VS, HD>(i, g + 8);
+        mo[(warp * 8 + 2 * c) * HD + da] = o[i][0];
+        mo[(warp * 8 + 2 * c + 1) * HD + da] = o[i][1];
+        mo[(warp * 8 + 2 * c) * HD + db] = o[i][2];
+        mo[(warp * 8 + 2 * c + 1) * HD + db] = o[i][3];
       }
     }
+    if (g == 0 && writer) {
+      ml[(warp * 8 + 2 * c) * 2] = m0;
+      ml[(warp * 8 + 2 * c) * 2 + 1] = l0;
+      ml[(warp * 8 + 2 * c + 1) * 2] = m1;
+      ml[(warp * 8 + 2 * c + 1) * 2 + 1] = l1;
+    }
+    __syncthreads();
+    float* red_s = reinterpret_cast<float*>(scan_s);       // [8 heads][m, l]
+    int* last_s = reinterpret_cast<int*>(scan_s + 8);
+    for (int idx = tid; idx < a.rep * HD; idx += NT) {
+      const int r = idx / HD, d = idx - r * HD;
+      float M = -CUDART_INF_F;
 #pragma unroll
-    for (int h = 0; h < NH; ++h)
-      pv16(sb + C::OFF_V + 16 * h * VT::VRS, sb + C::OFF_VS + 16 * h * VT::SROW, pw[h][0],
-           pw[h][1], pw[h][2], pw[h][3]);
-  }
-  cp_async_wait<0>();
+      for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, ml[(w2 * 8 + r) * 2]);
+      float acc = 0.f, lsum = 0.f;
+      if (M != -CUDART_INF_F) {
+#pragma unroll
+        for (int w2 = 0; w2 < NW; ++w2) {
+          const float f = exp2f(ml[(w2 * 8 + r) * 2] - M);
+          acc = fmaf(mo[(w2 * 8 + r) * HD + d], f, acc);
+          lsum = fmaf(ml[(w2 * 8 + r) * 2 + 1], f, lsum);
+        }
+      }
+      q_s[r * HD + d] = acc * a.v_mult;
+      if (d == 0) {
+        red_s[2 * r] = M;
+        red_s[2 * r + 1] = lsum;
+      }
+    }
+    __syncthreads();
+    const int64_t row0 = (int64_t)seq * a.nq + kvh * a.rep;
+    float* part0 = a.part + row0 * a.kmax * (HD + 4);
+    // Normalise row r of the unit, rotate it back when V is stored rotated
+    // and store it.
+    auto finish_row = [&](int r, float (&xr)[E], float lsum) {
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) xr[e] *= inv;
+      if constexpr (side_rotated(VS)) fwht_warp<E>(xr, lane, a.inv_sqrt_hd);
+      const int64_t o_ = (row0 + r) * HD + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (a.out_bf16) reinterpret_cast<uint16_t*>(a.out)[o_ + e] = bf16_bits_from_float(xr[e]);
+        else reinterpret_cast<float*>(a.out)[o_ + e] = xr[e];
+      }
+    };
+    if (np == 1) {  // the whole unit is here
+      for (int r = warp; r < a.rep; r += NW) {
+        float xr[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) xr[e] = q_s[r * HD + lane * E + e];
+        finish_row(r, xr, red_s[2 * r + 1]);
+      }
+    } else {
+      // Partial (m, l, acc) to slot `slot`; the last CTA of the unit to
+      // arrive merges all np of them (online-softmax identity) and returns
+      // the slots and the unit's counter to zero, so that the workspace is
+      // all zero between calls whatever their shapes.
+      for (int idx = tid; idx < a.rep * (HD + 4); idx += NT) {
+        const int r = idx / (HD + 4), d = idx - r * (HD + 4);
+        float v = 0.f;
+        if (d < 2) v = red_s[2 * r + d];
+        else if (d >= 4) v = q_s[r * HD + d - 4];
+        part0[((int64_t)r * a.kmax + slot) * (HD + 4) + d] = v;
+      }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        int* ctr = a.counters + (int64_t)seq * nkv + kvh;
+        const int prev = atomicAdd(ctr, 1);
+        *last_s = prev == np - 1;
+        if (prev == np - 1) *ctr = 0;
+      }
+      __syncthreads();
+      if (*last_s) {
+        __threadfence();
+        for (int r = warp; r < a.rep; r += NW) {
+          const float* pr = part0 + (int64_t)r * a.kmax * (HD + 4);
+          float mm = -CUDART_INF_F;
+          for (int i = 0; i < np; ++i) mm = fmaxf(mm, __ldcg(pr + i * (HD + 4)));
+          float xr[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) xr[e] = 0.f;
+          float ll = 0.f;
+          if (mm != -CUDART_INF_F) {
+            for (int i = 0; i < np; ++i) {
+              const float* pi = pr + i * (HD + 4);
+              const float w = exp2f(__ldcg(pi) - mm);
+              ll = fmaf(__ldcg(pi + 1), w, ll);
+#pragma unroll
+              for (int e = 0; e < E; ++e) xr[e] = fmaf(__ldcg(pi + 4 + lane * E + e), w, xr[e]);
+            }
+          }
+          finish_row(r, xr, ll);
+          float* pz = part0 + (int64_t)r * a.kmax * (HD + 4);
+          for (int i = lane; i < np * (HD + 4); i += 32) pz[i] = 0.f;
+        }
+      }
+    }
 
-#pragma unroll
-  for (int msk = 4; msk < 32; msk <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
-  }
-  if constexpr (PK) {  // P-hi columns + P-lo columns (lanes c, c ^ 2)
-#pragma unroll
-    for (int i = 0; i < NK; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[i][e] += __shfl_xor_sync(0xffffffffu, o[i][e], 2);
-  }
-  const bool writer = !PK || c < 2;
-  __syncthreads();  // every warp is done with its ring
-  float* mo = reinterpret_cast<float*>(rings);   // [NW warps][8 heads][HD]
-  float* ml = mo + NW * 8 * HD;                  // [NW warps][8 heads][m, l]
-  if (writer) {
-#pragma unroll
-    for (int i = 0; i < NK; ++i) {
-      const int da = v_row_dim<VS, HD>(i, g), db = v_row_dim<VS, HD>(i, g + 8);
-      mo[(warp * 8 + 2 * c) * HD + da] = o[i][0];
-      mo[(warp * 8 + 2 * c + 1) * HD + da] = o[i][1];
-      mo[(warp * 8 + 2 * c) * HD + db] = o[i][2];
-      mo[(warp * 8 + 2 * c + 1) * HD + db] = o[i][3];
-    }
-  }
-  if (g == 0 && writer) {
-    ml[(warp * 8 + 2 * c) * 2] = m0;
-    ml[(warp * 8 + 2 * c) * 2 + 1] = l0;
-    ml[(warp * 8 + 2 * c + 1) * 2] = m1;
-    ml[(warp * 8 + 2 * c + 1) * 2 + 1] = l1;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < a.rep * HD; idx += NT) {
-    const int r = idx / HD, d = idx - r * HD;
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, ml[(w2 * 8 + r) * 2]);
-    float acc = 0.f, lsum = 0.f;
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int w2 = 0; w2 < NW; ++w2) {
-        const float f = exp2f(ml[(w2 * 8 + r) * 2] - M);
-        acc = fmaf(mo[(w2 * 8 + r) * HD + d], f, acc);
-        lsum = fmaf(ml[(w2 * 8 + r) * 2 + 1], f, lsum);
-      }
-    }
-    float* pp = part + r * pstride;
-    pp[4 + d] = acc * a.v_mult;
-    if (d == 0) {
-      pp[0] = M;
-      pp[1] = lsum;
+    // next unit
+    x += take;
+    off = 0;
+    if (++kvh == nkv) {
+      kvh = 0;
+      int f2, n2 = 0, l2, e2;
+      do {
+        ++seq;
+        if (seq >= N) break;
+        seq_slabs(seq, f2, n2, l2, e2);
+      } while (n2 == 0);
     }
   }
 }
@@ -860,7 +1047,9 @@ cudaError_t launch_tc_kern(const DecodeArgs& a, const Codebooks& cb, cudaStream_
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(a.nsplit, a.nkv, a.num_seqs);
+  // a.grid is two CTAs per SM; instances whose stages need more than half
+  // of an SM's shared memory run one per SM.
+  const int grid = C::SMEM <= 113 * 1024 ? a.grid : (a.grid + 1) / 2;
   kern<<<grid, 32 * C::NW, C::SMEM, st>>>(a, cb);
   return cudaGetLastError();
 }

@@ -30,7 +30,7 @@ struct WriteArgs {
   int32_t* err;
 };
 
-struct DecodeArgs {  // arguments of the split-K decode (decode_tc_kernel)
+struct DecodeArgs {  // arguments of the paged decode (decode_tc_kernel)
   const void* q;
   int64_t q_stride;       // elements between sequences
   int q_bf16;
@@ -49,25 +49,19 @@ struct DecodeArgs {  // arguments of the split-K decode (decode_tc_kernel)
   float inv_sqrt_hd;
   int32_t window;
   float sparse_thr;
-  int32_t pages_per_split;
-  int32_t nsplit;
-  float* part;            // [num_seqs][nq][nsplit][head_dim + 4] fp32
+  int32_t grid;           // persistent CTAs: two per SM (halved by the launcher when one fits)
+  int32_t min_slabs;      // lower bound of the slabs per CTA
+  int32_t kmax;           // partial slots per (sequence, query head)
+  float* part;            // [num_seqs][nq][kmax][head_dim + 4] fp32: m, l, -, -, acc[head_dim]
+  int32_t* counters;      // [num_seqs][nkv] partials arrived; zero between calls
+  void* out;              // [num_seqs][nq][head_dim], fp32 or bf16
+  int out_bf16;
   int32_t* err;
 };
 
-struct CombineArgs {
-  const float* part;
-  void* out;
-  int out_bf16;
-  int32_t num_seqs, nq, nsplit;
-  int v_rotated;
-  float inv_sqrt_hd;
-};
 
 cudaError_t launch_cache_write(const WriteArgs& a, const Codebooks& cb, int head_dim,
                                bool in_bf16, bool vec, int grid, cudaStream_t st);
-
-cudaError_t launch_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
 
 // Tensor-core decode (kvq_decode_tc_k_*.cu) for the pairs it supports.
 bool decode_tc_supported(int k_side, int v_side);

@@ -1,7 +1,7 @@
 // Paged decode for callers that cannot allocate device memory.
 //
-// kvq_paged_decode needs a caller-provided scratch buffer for its split-K
-// partial results.  Some callers cannot get one: a runtime that has already
+// kvq_paged_decode needs a caller-provided scratch buffer for the partial
+// results of rows that several CTAs share and their merge counters.  Some callers cannot get one: a runtime that has already
 // handed all device memory to its own pool, a plugin host that forbids
 // device allocations by its plugins, or a latency-critical loop where
 // cudaMalloc (which may synchronize the device) is not acceptable.  This
@@ -13,9 +13,9 @@
 // the host it only names a stand-in); the device address is looked up with
 // cudaGetSymbolAddress once per device, on the first call made with that
 // device current, and cached.  Make that first call before any stream
-// capture.  All calls share the one array and the decode leaves its
-// partials there, so calls whose kernels overlap on the GPU race; the
-// decode writes every partial before reading it, so nothing needs clearing.
+// capture.  All calls share the one array, so calls whose kernels overlap on
+// the GPU race.  The array is zero when the library loads (static storage)
+// and every decode leaves it zero, which is the state the next call needs.
 #include "../../include/kvq.h"
 
 #include <cuda_runtime.h>

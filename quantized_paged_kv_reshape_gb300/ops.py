@@ -78,7 +78,7 @@ def alloc_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                     max_blocks_per_seq, sliding_window, fmt, device="cuda"):
     n = decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                max_blocks_per_seq, sliding_window, fmt)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
 def paged_decode(q, k_cache, v_cache, block_tables, seq_lens, fmt, num_kv_heads,

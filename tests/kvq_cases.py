@@ -68,7 +68,7 @@ def oracle_decode(c, window=0, sparse=0.0, q=None):
 
 
 def gpu_decode(c, window=0, sparse=0.0, dev="cuda", out_dtype=torch.float32, q_dtype=None,
-               err=None):
+               err=None, workspace=None):
     kpool = torch.from_numpy(c["kc"].reshape(c["num_blocks"], c["kst"])).to(dev)
     vpool = torch.from_numpy(c["vc"].reshape(c["num_blocks"], c["vst"])).to(dev)
     qd = q_dtype or (torch.bfloat16 if c["in_dtype"] == "bf16" else torch.float32)
@@ -76,7 +76,8 @@ def gpu_decode(c, window=0, sparse=0.0, dev="cuda", out_dtype=torch.float32, q_d
     out = ops.paged_decode(q, kpool, vpool, torch.from_numpy(c["tables"]).to(dev),
                            torch.from_numpy(c["lens"]).to(dev), c["fmt"], c["nkv"], c["bs"],
                            out_dtype=out_dtype, k_scale=c["k_scale"], v_scale=c["v_scale"],
-                           sliding_window=window, sparse_v_threshold=sparse, error_flag=err)
+                           sliding_window=window, sparse_v_threshold=sparse, error_flag=err,
+                           workspace=workspace)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64)
 

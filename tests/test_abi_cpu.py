@@ -128,6 +128,15 @@ def test_decode_rejects_bad_arguments():
 
 
 def test_workspace_formula():
+    """Partials [num_seqs][nq][kmax][hd + 4] fp32, then int32 partial counts
+    [num_seqs][nkv] (16-byte padded); kmax >= 2 (a unit cut once) and never
+    above floor((slabs - 1) / 16) + 2 for a sequence of `slabs` 16-token slabs."""
+    counts = 32 * 8 * 4
     n = A.kvq_decode_workspace_bytes(32, 32, 8, 128, 16, 256, 0, 0)
-    assert n > 0 and n % (32 * 32 * (128 + 4) * 4) == 0
+    row = 32 * 32 * (128 + 4) * 4
+    assert n > counts and (n - counts) % row == 0
+    assert 2 <= (n - counts) // row <= (256 - 1) // 16 + 2
+    # a 40-token window bounds the slabs at 4, hence kmax at 2
+    n = A.kvq_decode_workspace_bytes(32, 32, 8, 128, 16, 256, 40, 0)
+    assert n == 2 * row + counts
     assert A.kvq_decode_workspace_bytes(32, 32, 8, 128, 24, 256, 0, 0) == 0

@@ -12,6 +12,7 @@ import torch
 
 from kvq_cases import (ALL_FORMATS, assert_decode_close, decode_case, gpu_decode,
                        oracle_decode)
+from quantized_paged_kv_reshape_gb300 import ops
 
 pytestmark = pytest.mark.gpu
 
@@ -92,3 +93,25 @@ def test_decode_flags_bad_block():
     assert np.isfinite(got).all()
     ref = oracle_decode(dict(c, tables=c["tables"][:1], lens=c["lens"][:1], q=c["q"][:1]))
     assert_decode_close(got[:1], ref)
+
+
+def test_decode_workspace_reuse_leaves_zero():
+    """One workspace, zeroed once, for decodes of different formats, shapes and
+    lengths in a row (twice over): each matches the oracle and leaves the
+    workspace all zero.  The long rows span many CTAs, so their partial slots
+    and merge counters are used; the short ones finish inside one CTA."""
+    specs = [("turbo4", [3000, 40, 0, 777], 8, 2, 128, 0),
+             ("bf16", LENS, 8, 2, 64, 0),
+             ("fp8k_turbo2v", [5000], 16, 2, 128, 0),
+             ("turbo8", [900, 12], 4, 2, 256, 0),
+             ("turbo4k_turbo3v", [4000, 2500], 8, 2, 128, 600)]
+    cases = [(decode_case(f, lens, nq, nkv, hd, seed=i), win)
+             for i, (f, lens, nq, nkv, hd, win) in enumerate(specs)]
+    need = max(ops.decode_workspace_bytes(len(c["lens"]), c["nq"], c["nkv"], c["hd"], c["bs"],
+                                          c["tables"].shape[1], win, c["fmt"])
+               for c, win in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        for c, win in cases:
+            assert_decode_close(gpu_decode(c, window=win, workspace=ws), oracle_decode(c, window=win))
+            assert int(torch.count_nonzero(ws)) == 0
