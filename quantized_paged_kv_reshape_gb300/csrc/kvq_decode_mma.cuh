@@ -199,7 +199,8 @@ struct TcCfg {
   static constexpr int OFF_BLK = 8 * HD * 4;                   // after q_s [8][HD] fp32
   static constexpr int OFF_OFFS = OFF_BLK + MAXP * 4;          // int32 block ids of a stretch
   static constexpr int OFF_SCAN = OFF_OFFS + NW * 128 * 8;     // per-warp row offsets
-  static constexpr int OFF_LUT = OFF_SCAN + 16 * 8;            // partition scan scratch
+  static constexpr int OFF_STATE = OFF_SCAN + 16 * 8;          // partition scan / merge scratch
+  static constexpr int OFF_LUT = OFF_STATE + 8 * 8;            // CTA loop state
   static constexpr int OFF_RING = OFF_LUT + LUTS;
   static constexpr int BUDGET = 112 * 1024 - OFF_RING;         // two CTAs per SM
   static constexpr int NST0 = BUDGET / (NW * STAGE);
@@ -739,36 +740,58 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   };
 
 
-  // ---- the units of this CTA's slab range
-  int64_t x = x0;
-  while (x < x_end && seq < N) {
-    int first, n, len;
-    seq_slabs(seq, first, n, lo, len);
-    const int64_t take = min((int64_t)n - off, x_end - x);
-    const int64_t ou = x - off;                            // the unit's first slab
-    const int slot = (int)(blockIdx.x - ou / cpc);         // this CTA's partial
-    const int np = (int)((ou + n - 1) / cpc - ou / cpc + 1);  // CTAs on the unit
-    tab = (int64_t)seq * a.max_blocks;
+  // ---- the units of this CTA's slab range.  The CTA-uniform loop state
+  // lives in shared memory (re-read after each barrier), so that the slab
+  // loop keeps only what it uses in registers.
+  int64_t* st = reinterpret_cast<int64_t*>(smem + C::OFF_STATE);
+  // st: 0 x (next slab of the range), 1 x_end, 2 seq, 3 kvh, 4 off (slab of
+  // the unit at x), 5 next stretch, 6 end of the unit's slabs here, 7 cpc
+  if (tid == 0) {
+    st[0] = x0;
+    st[1] = x_end;
+    st[2] = seq;
+    st[3] = kvh;
+    st[4] = off;
+    st[7] = cpc;
+  }
+  for (;;) {
+    __syncthreads();  // loop state visible; the previous unit's merge is done
+    {
+      const int64_t x = st[0];
+      if (x >= st[1]) break;
+      int first, n, len;
+      seq_slabs((int)st[2], first, n, lo, len);
+      if (tid == 0) {
+        st[5] = first + st[4];
+        st[6] = first + st[4] + min((int64_t)n - st[4], st[1] - x);
+      }
+    }
 #pragma unroll
     for (int i = 0; i < NK; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     m0 = m1 = -CUDART_INF_F;
     l0 = l1 = 0.f;
     // Stretches of at most MAXP pages (the staged block ids).
-    const int sub = (C::MAXP - 1) * bs / SLAB;
-    const int64_t s_lo = first + off, s_hi = first + off + take;
-    for (int64_t sa = s_lo; sa < s_hi; sa += sub) {
+    for (int first_stretch = 1;; first_stretch = 0) {
+      __syncthreads();  // blk_s, q_s and the rings are free; st[5] visible
+      const int64_t sa = st[5], s_hi = st[6];
+      if (sa >= s_hi) break;
+      const int sq = (int)st[2];
+      kvh = (int)st[3];
+      int first, n, len;
+      seq_slabs(sq, first, n, lo, len);
+      const int sub = (C::MAXP - 1) * bs / SLAB;
       const int nsl = (int)min((int64_t)sub, s_hi - sa);
       tok0 = (int)(sa * SLAB);
       tok_end = min(tok0 + nsl * SLAB, len);
       p0 = tok0 >> lbs;
       const int p1 = ((tok_end - 1) >> lbs) + 1;
-      __syncthreads();  // blk_s, q_s and the rings are free
-      if (sa == s_lo) {
+      tab = (int64_t)sq * a.max_blocks;
+      if (first_stretch) {
         // ---- queries (rotated when K is stored rotated), rows >= rep are zero
         for (int j = warp; j < 8; j += NW) {
           float xq[E];
           if (j < a.rep) {
-            const int64_t qoff = (int64_t)seq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
+            const int64_t qoff = (int64_t)sq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
 #pragma unroll
             for (int i = 0; i < E; ++i)
               xq[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
@@ -790,13 +813,14 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
         blk_s[i] = bad ? -1 : (int)b;
       }
       __syncthreads();
+      if (tid == 0) st[5] = sa + nsl;
       const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
 #pragma unroll
       for (int s = 0; s < C::NST - 1; ++s) {
         if (s < my) issue(s);
         cp_async_commit();
       }
-      if (sa == s_lo) {
+      if (first_stretch) {
 #pragma unroll
         for (int j = 0; j < NK; ++j) {
           int d[4];
@@ -898,6 +922,15 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       cp_async_wait<0>();
     }
 
+    // ---- merge of the unit's warps; the unit's parameters again from st
+    const int64_t x = st[0], off_u = st[4];
+    const int seq_u = (int)st[2], kvh_u = (int)st[3];
+    int first_u, n_u, len_u, lo_u;
+    seq_slabs(seq_u, first_u, n_u, lo_u, len_u);
+    const int64_t take = min((int64_t)n_u - off_u, st[1] - x);
+    const int64_t ou = x - off_u, cp = st[7];                  // the unit's first slab
+    const int slot = (int)(blockIdx.x - ou / cp);              // this CTA's partial
+    const int np = (int)((ou + n_u - 1) / cp - ou / cp + 1);   // CTAs on the unit
 #pragma unroll
     for (int msk = 4; msk < 32; msk <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
@@ -953,7 +986,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       }
     }
     __syncthreads();
-    const int64_t row0 = (int64_t)seq * a.nq + kvh * a.rep;
+    const int64_t row0 = (int64_t)seq_u * a.nq + kvh_u * a.rep;
     float* part0 = a.part + row0 * a.kmax * (HD + 4);
     // Normalise row r of the unit, rotate it back when V is stored rotated
     // and store it.
@@ -991,7 +1024,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       __threadfence();
       __syncthreads();
       if (tid == 0) {
-        int* ctr = a.counters + (int64_t)seq * nkv + kvh;
+        int* ctr = a.counters + (int64_t)seq_u * nkv + kvh_u;
         const int prev = atomicAdd(ctr, 1);
         *last_s = prev == np - 1;
         if (prev == np - 1) *ctr = 0;
@@ -1024,16 +1057,22 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     }
 
     // next unit
-    x += take;
-    off = 0;
-    if (++kvh == nkv) {
-      kvh = 0;
-      int f2, n2 = 0, l2, e2;
-      do {
-        ++seq;
-        if (seq >= N) break;
-        seq_slabs(seq, f2, n2, l2, e2);
-      } while (n2 == 0);
+    if (tid == 0) {
+      int s2 = seq_u, h2 = kvh_u + 1;
+      if (h2 == nkv) {
+        h2 = 0;
+        int f2, n2 = 0, l2, e2;
+        do {
+          ++s2;
+          if (s2 >= N) break;
+          seq_slabs(s2, f2, n2, l2, e2);
+        } while (n2 == 0);
+      }
+      st[0] = x + take;
+      st[2] = s2 < N ? s2 : N - 1;
+      st[3] = h2;
+      st[4] = 0;
+      if (s2 >= N) st[1] = st[0];  // nothing left
     }
   }
 }
