@@ -343,12 +343,18 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     n = ((len + 15) >> 4) - first;
   };
 
-  // ---- Partition.  The (sequence, kv head) units, sequence-major, are laid
-  // end to end in slabs (T in all); CTA b takes slabs [b * cpc, (b + 1) *
-  // cpc), cpc = max(ceil(T / gridDim), min_slabs), so every CTA gets the same
-  // amount of work whatever the lengths.  A unit cut by CTA boundaries leaves
-  // one partial per CTA, in slot (CTA - first CTA of the unit).
+  // ---- Partition.  Each kv head gets R = gridDim.x / nkv CTAs (the host
+  // launches a multiple of nkv).  The sequences' 16-token slabs are laid end
+  // to end (S in all); CTA (h, j) takes slabs [j * cpc, (j + 1) * cpc) of
+  // kv head h, cpc = max(ceil(S / R), min_slabs), so every CTA gets the same
+  // amount of work whatever the lengths, and the CTAs of the different kv
+  // heads read the same token positions at the same time (their rows share
+  // DRAM sectors, the scale rows especially).  A (sequence, kv head) row cut
+  // by CTA boundaries leaves one partial per CTA, in slot (j - first j of
+  // the row).
   const int N = a.num_seqs;
+  const int R = gridDim.x / nkv;
+  const int kvh = blockIdx.x / R, jr = blockIdx.x - kvh * R;
   const int chunk = (N + NT - 1) / NT;
   const int s_beg = min(N, tid * chunk), s_end = min(N, s_beg + chunk);
   int64_t mine = 0;
@@ -372,12 +378,11 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     if (w2 < warp) before += v;
     total += v;
   }
-  const int64_t excl = before + incl - mine;  // slabs of one kv head before this chunk
-  const int64_t T = total * nkv;
-  int64_t cpc = (T + gridDim.x - 1) / gridDim.x;
+  const int64_t excl = before + incl - mine;  // slabs before this thread's chunk
+  int64_t cpc = (total + R - 1) / R;
   if (cpc < a.min_slabs) cpc = a.min_slabs;
-  const int64_t x0 = (int64_t)blockIdx.x * cpc;
-  const int64_t x_end = min(x0 + cpc, T);
+  const int64_t x0 = (int64_t)jr * cpc;
+  const int64_t x_end = min(x0 + cpc, total);
   __syncthreads();  // scan_s is reused below
   if (blockIdx.x == 0) {  // sequences with nothing to attend get zero rows
     for (int s = s_beg; s < s_end; ++s) {
@@ -391,25 +396,23 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       }
     }
   }
-  if (x0 < T && nkv * excl <= x0 && x0 < nkv * (excl + mine)) {  // the chunk holding x0
+  if (kvh < nkv && x0 < total && excl <= x0 && x0 < excl + mine) {  // the chunk holding x0
     int64_t P = excl;
     for (int s = s_beg; s < s_end; ++s) {
       int f, n, l_, e_;
       seq_slabs(s, f, n, l_, e_);
-      if (x0 < nkv * (P + n)) {
-        const int64_t r = x0 - nkv * P;
+      if (x0 < P + n) {
         scan_s[0] = s;
-        scan_s[1] = r / n;
-        scan_s[2] = r % n;
+        scan_s[1] = x0 - P;
         break;
       }
       P += n;
     }
   }
   __syncthreads();
-  if (x0 >= T) return;
-  int seq = (int)scan_s[0], kvh = (int)scan_s[1];
-  int64_t off = scan_s[2];
+  if (kvh >= nkv || x0 >= total) return;
+  int seq = (int)scan_s[0];
+  int64_t off = scan_s[1];
 
   // Pair LUTs of the codebook sides: entry p = (code of dim 2k) | (code of
   // dim 2k+1) << b holds fp16 (hi, hi) and (lo, lo) where hi and lo carry 7
@@ -744,13 +747,12 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   // lives in shared memory (re-read after each barrier), so that the slab
   // loop keeps only what it uses in registers.
   int64_t* st = reinterpret_cast<int64_t*>(smem + C::OFF_STATE);
-  // st: 0 x (next slab of the range), 1 x_end, 2 seq, 3 kvh, 4 off (slab of
-  // the unit at x), 5 next stretch, 6 end of the unit's slabs here, 7 cpc
+  // st: 0 x (next slab of the range), 1 x_end, 2 seq, 4 off (slab of the
+  // row at x), 5 next stretch, 6 end of the row's slabs here, 7 cpc
   if (tid == 0) {
     st[0] = x0;
     st[1] = x_end;
     st[2] = seq;
-    st[3] = kvh;
     st[4] = off;
     st[7] = cpc;
   }
@@ -776,7 +778,6 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       const int64_t sa = st[5], s_hi = st[6];
       if (sa >= s_hi) break;
       const int sq = (int)st[2];
-      kvh = (int)st[3];
       int first, n, len;
       seq_slabs(sq, first, n, lo, len);
       const int sub = (C::MAXP - 1) * bs / SLAB;
@@ -924,12 +925,12 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
 
     // ---- merge of the unit's warps; the unit's parameters again from st
     const int64_t x = st[0], off_u = st[4];
-    const int seq_u = (int)st[2], kvh_u = (int)st[3];
+    const int seq_u = (int)st[2], kvh_u = kvh;
     int first_u, n_u, len_u, lo_u;
     seq_slabs(seq_u, first_u, n_u, lo_u, len_u);
     const int64_t take = min((int64_t)n_u - off_u, st[1] - x);
     const int64_t ou = x - off_u, cp = st[7];                  // the unit's first slab
-    const int slot = (int)(blockIdx.x - ou / cp);              // this CTA's partial
+    const int slot = (int)(jr - ou / cp);                      // this CTA's partial
     const int np = (int)((ou + n_u - 1) / cp - ou / cp + 1);   // CTAs on the unit
 #pragma unroll
     for (int msk = 4; msk < 32; msk <<= 1) {
@@ -1057,20 +1058,16 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     }
 
     // next unit
-    if (tid == 0) {
-      int s2 = seq_u, h2 = kvh_u + 1;
-      if (h2 == nkv) {
-        h2 = 0;
-        int f2, n2 = 0, l2, e2;
-        do {
-          ++s2;
-          if (s2 >= N) break;
-          seq_slabs(s2, f2, n2, l2, e2);
-        } while (n2 == 0);
-      }
+    if (tid == 0) {  // next sequence with positions to attend
+      int s2 = seq_u, n2 = 0;
+      do {
+        ++s2;
+        if (s2 >= N) break;
+        int f2, l2, e2;
+        seq_slabs(s2, f2, n2, l2, e2);
+      } while (n2 == 0);
       st[0] = x + take;
       st[2] = s2 < N ? s2 : N - 1;
-      st[3] = h2;
       st[4] = 0;
       if (s2 >= N) st[1] = st[0];  // nothing left
     }
@@ -1086,9 +1083,10 @@ cudaError_t launch_tc_kern(const DecodeArgs& a, const Codebooks& cb, cudaStream_
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
   }
-  // a.grid is two CTAs per SM; instances whose stages need more than half
-  // of an SM's shared memory run one per SM.
-  const int grid = C::SMEM <= 113 * 1024 ? a.grid : (a.grid + 1) / 2;
+  // a.ranges CTAs per kv head fill two CTAs per SM; instances whose stages
+  // need more than half of an SM's shared memory run one per SM.
+  const int ranges = C::SMEM <= 113 * 1024 ? a.ranges : (a.ranges + 1) / 2;
+  const int grid = ranges * a.nkv;
   kern<<<grid, 32 * C::NW, C::SMEM, st>>>(a, cb);
   return cudaGetLastError();
 }
