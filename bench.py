@@ -54,7 +54,11 @@ WORKLOAD_DESC = {
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # decode launch, from the ncu capture summarised in profiles/ (None when the
 # kernel changed after the capture).
-TRAFFIC = {}
+TRAFFIC = {
+    ("llama8b", "bf16"): 542_208_768,
+    ("llama8b", "fp8"): 273_052_928,
+    ("llama8b", "turbo4"): 156_112_896,
+}
 
 
 def peaks():
