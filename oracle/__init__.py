@@ -27,11 +27,11 @@ from .formats import (  # noqa: F401
 )
 from .codebook import lloyd_max_gaussian, codebook, distortion  # noqa: F401
 from .numformats import (  # noqa: F401
-    e4m3_decode, e4m3_encode, bf16_encode, bf16_decode,
+    e4m3_decode, e4m3_encode, bf16_encode, bf16_decode, e2m1_decode, e2m1_encode,
 )
 from .wht import fwht_f32, wht_f64  # noqa: F401
 from .cache_write import (  # noqa: F401
-    quantize_rows, quantize_rotated, pack_codes, unpack_codes, encode_rows_bytes,
+    quantize_rows, quantize_rotated, quantize_nvfp4, pack_codes, unpack_codes, encode_rows_bytes,
     cache_write,
 )
 from .decode import dequantize_rows, gather_side, paged_decode  # noqa: F401

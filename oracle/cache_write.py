@@ -12,6 +12,13 @@ What it computes, per (token t, kv head h) row x of head_dim elements:
   smallest positive level) for every element; it dequantizes to 0.
 * ``turbo8`` : y = WHT(x); s = BF16(amax_g / 448) per group; data byte =
   E4M3(y / s) (fp32 divide); a zero scale stores data byte 0x00.
+* ``nvfp4``  : no rotation; per 16-element group g of x: scale byte =
+  E4M3(amax_g / 6) (fp32 divide, 6 = the largest E2M1 magnitude), s = its
+  value; per element: code = E2M1(x / s) (fp32 divide, RNE, saturating);
+  a group whose scale byte decodes to 0 stores code 0 (dequantizes to 0).
+  Packed and laid out exactly like turbo4 ("spark_runtime/kv_cache.rs",
+  ``block_bytes_dims``: "Same byte layout, different codebook (E2M1 vs
+  Lloyd-Max)").
 
 Layout of one block of one side ("metrale_model_layers/.../
 kv_cache_bf16k_turbov.rs", module invariants; "spark_runtime/kv_cache.rs",
@@ -41,7 +48,8 @@ import numpy as np
 
 from . import formats as F
 from .codebook import codebook, quantize_unit
-from .numformats import bf16_encode, e4m3_decode, e4m3_encode, bf16_decode
+from .numformats import (bf16_encode, e4m3_decode, e4m3_encode, bf16_decode, e2m1_encode,
+                         E2M1_MAX)
 from .wht import fwht_f32
 
 
@@ -75,6 +83,21 @@ def quantize_rotated(side, y):
     return codes.reshape(r, hd), s_byte
 
 
+def quantize_nvfp4(x):
+    """NVFP4 rows x [R, hd] (original basis): (uint8 E2M1 codes [R, hd],
+    uint8 E4M3 scale bytes [R, hd/16])."""
+    x = np.asarray(x, dtype=np.float32)
+    r, hd = x.shape
+    g = x.reshape(r, hd // F.GROUP, F.GROUP)
+    amax = np.max(np.abs(g), axis=-1)
+    s_byte = e4m3_encode(amax / np.float32(E2M1_MAX))
+    s = e4m3_decode(s_byte).astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = g / s
+    codes = np.where(s == 0, np.uint8(0), e2m1_encode(v)).astype(np.uint8)
+    return codes.reshape(r, hd), s_byte
+
+
 def quantize_rows(side, x, scale=None):
     """Encode rows ``x`` [R, hd] (fp32) of one side.
 
@@ -90,6 +113,8 @@ def quantize_rows(side, x, scale=None):
     if side == F.FP8:
         s = np.float32(scale)
         return e4m3_encode(x / s), None
+    if side == F.NVFP4:
+        return quantize_nvfp4(x)
     return quantize_rotated(side, fwht_f32(x))
 
 

@@ -11,7 +11,8 @@ The plain definition, in fp64:
    ("combs_models/kv.rs", ``PagedKVCache::attention`` / ``gather_window``).
 2. Each stored K/V row is dequantized from the cache bytes to fp64:
    bf16 -> its value; fp8 -> E4M3 value * per-tensor scale; turbo{2,3,4} ->
-   level[code] * E4M3 group scale; turbo8 -> E4M3 value * BF16 group scale.
+   level[code] * E4M3 group scale; turbo8 -> E4M3 value * BF16 group scale;
+   nvfp4 -> E2M1 value * E4M3 group scale (not rotated).
    Rows stored in the Walsh-Hadamard basis ("spark_runtime/kv_cache.rs",
    ``is_wht_rotated``) are rotated back with the fp64 WHT (its own inverse),
    so attention below runs on K and V in the original basis; the kernel's
@@ -38,7 +39,7 @@ import numpy as np
 
 from . import formats as F
 from .codebook import codebook
-from .numformats import bf16_decode, e4m3_decode
+from .numformats import bf16_decode, e2m1_decode, e4m3_decode
 from .cache_write import unpack_codes
 from .wht import wht_f64
 
@@ -59,10 +60,13 @@ def dequantize_rows(side, data, scales, hd, scale=None):
         vals = e4m3_decode(data).reshape(r, ng, F.GROUP)
         return (vals * s[..., None]).reshape(r, hd)
     bits = F.CODE_BITS[side]
-    lv64, _, _ = codebook(bits)
     codes = unpack_codes(data, bits, hd)
     s = e4m3_decode(np.asarray(scales, np.uint8).reshape(r, ng))
-    vals = lv64[codes].reshape(r, ng, F.GROUP)
+    if side == F.NVFP4:
+        vals = e2m1_decode(codes).reshape(r, ng, F.GROUP)
+    else:
+        lv64, _, _ = codebook(bits)
+        vals = lv64[codes].reshape(r, ng, F.GROUP)
     return (vals * s[..., None]).reshape(r, hd)
 
 

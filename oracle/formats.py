@@ -56,7 +56,7 @@ _ALIASES = {
 }
 
 # Bits per stored code for the codebook sides.
-CODE_BITS = {TURBO4: 4, TURBO3: 3, TURBO2: 2}
+CODE_BITS = {TURBO4: 4, TURBO3: 3, TURBO2: 2, NVFP4: 4}
 
 
 def format_from_string(s):

@@ -18,10 +18,19 @@ bit-twiddles, so the encoder is checkable by eye against the definition.
 BF16: the upper 16 bits of an IEEE fp32 pattern.  Encoding rounds the fp32
 value to the nearest bf16, ties to even mantissa.
 
+E2M1 (the 4-bit element of NVFP4, "spark_runtime/kv_cache.rs" ``Nvfp4``:
+"E2M1 packed nibbles"): 1 sign bit (bit 3), 2 exponent bits (bias 1), 1
+mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 for codes 0..7; no
+infinities or NaN.  Encoding is again "pick the nearest representable
+magnitude", ties to the even code, saturating at 6, sign from the sign bit of
+the input (the pages name the format only; RNE-saturate is the reading).
+
 Pins (tests/test_oracle_numformats.py): all 256 E4M3 codes against torch's
 float8_e4m3fn view (a library special case); encoding against torch's RNE
 cast inside the finite range; hand-checked saturation, subnormal and tie
-cases; BF16 against torch's bfloat16 cast.
+cases; BF16 against torch's bfloat16 cast; the 16 E2M1 codes and their
+midpoint ties by hand, and the E2M1 encoder against torch's float4_e2m1fn_x2
+where that dtype exists.
 """
 
 import numpy as np
@@ -92,3 +101,42 @@ def bf16_decode(bits):
     """fp32 values of uint16 BF16 patterns (exact)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32)
+
+
+E2M1_MAX = 6.0
+
+
+def e2m1_decode(codes):
+    """fp64 values of 4-bit E2M1 codes (uint8 holding 0..15)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64) & 0xF
+    sign = np.where(c & 0x8, -1.0, 1.0)
+    exp = (c >> 1) & 0x3
+    man = c & 0x1
+    mag = np.where(exp == 0, man * 0.5, (1.0 + man / 2.0) * np.power(2.0, exp - 1.0))
+    return sign * mag
+
+
+_E2M1_POS_CODES = np.arange(8, dtype=np.uint8)
+_E2M1_POS_VALUES = e2m1_decode(_E2M1_POS_CODES)
+assert np.all(np.diff(_E2M1_POS_VALUES) > 0)
+
+
+def e2m1_encode(x):
+    """4-bit E2M1 codes (uint8 0..15) of fp32/fp64 values: RNE, saturating.
+
+    The sign bit follows the input's sign bit (-0.0 and negatives that round
+    to zero give 0x8).  NaN is not expected (the callers divide finite values
+    by nonzero scales) and maps to 0x7.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.minimum(np.abs(x), E2M1_MAX)
+    hi_idx = np.searchsorted(_E2M1_POS_VALUES, mag, side="left")
+    hi_idx = np.minimum(hi_idx, len(_E2M1_POS_VALUES) - 1)
+    lo_idx = np.where(_E2M1_POS_VALUES[hi_idx] == mag, hi_idx, np.maximum(hi_idx - 1, 0))
+    d_lo = mag - _E2M1_POS_VALUES[lo_idx]
+    d_hi = _E2M1_POS_VALUES[hi_idx] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi_idx % 2 == 0) & (hi_idx != lo_idx))
+    code = np.where(pick_hi, hi_idx, lo_idx).astype(np.uint8)
+    code = np.where(np.signbit(x), code | np.uint8(0x8), code).astype(np.uint8)
+    code = np.where(np.isnan(x), np.uint8(0x7), code).astype(np.uint8)
+    return code

@@ -4,7 +4,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.numformats import bf16_decode, bf16_encode, e4m3_decode, e4m3_encode
+from oracle.numformats import (bf16_decode, bf16_encode, e2m1_decode, e2m1_encode,
+                               e4m3_decode, e4m3_encode)
 
 
 def test_e4m3_decode_all_codes_vs_torch():
@@ -62,3 +63,26 @@ def test_bf16_vs_torch():
     assert np.array_equal(bf16_encode(x), ref)
     assert np.array_equal(bf16_decode(bf16_encode(x)),
                           torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+
+
+def test_e2m1_decode_table():
+    """E2M1: sign bit 3, exponent bits 2-1 (bias 1), mantissa bit 0; exponent 0
+    is subnormal (0, 0.5).  Written out by hand."""
+    want = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    got = e2m1_decode(np.arange(16, dtype=np.uint8))
+    assert list(got[:8]) == want
+    assert list(-got[8:]) == want
+
+
+def test_e2m1_roundtrip_all_codes():
+    codes = np.arange(16, dtype=np.uint8)
+    assert np.array_equal(e2m1_encode(e2m1_decode(codes)), codes)   # -0.0 -> 0x8 too
+
+
+@pytest.mark.parametrize("x,code", [
+    (0.25, 0x0), (0.75, 0x2), (1.25, 0x2), (1.75, 0x4), (2.5, 0x4), (3.5, 0x6), (5.0, 0x6),
+    (0.26, 0x1), (0.74, 0x1), (1.26, 0x3), (4.99, 0x6), (5.01, 0x7), (6.0, 0x7), (1e9, 0x7),
+    (-0.25, 0x8), (-0.3, 0x9), (-5.01, 0xF), (0.0, 0x0), (-0.0, 0x8), (1e-30, 0x0)])
+def test_e2m1_points(x, code):
+    """Midpoints go to the even code; beyond 6 saturates; sign from the sign bit."""
+    assert int(e2m1_encode(np.float32(x))) == code

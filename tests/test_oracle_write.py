@@ -1,7 +1,9 @@
 """Pins of the oracle's cache write.
 
 * Hand-worked groups (tests/golden/turbo_groups.txt, derived by hand from the
-  format descriptions of "spark_runtime/kv_cache.rs").
+  format descriptions of "spark_runtime/kv_cache.rs"), NVFP4 included.
+* "Turbo4 ~2x lower MSE than NVFP4 at the same bit rate" ("spark_runtime/
+  kv_cache.rs", KvCacheDtype::Turbo4): the direction and a loose band.
 * Packing: brute-force round trips and an independent big-integer packing.
 * Layout: the [num_blocks, block_size, num_kv_heads, head_dim] layout of the
   "metrale_model_layers/.../kv_cache_bf16k_turbov.rs" invariants read back
@@ -15,7 +17,7 @@ import numpy as np
 import pytest
 
 import oracle.formats as F
-from oracle.cache_write import (cache_write, pack_codes, quantize_rotated,
+from oracle.cache_write import (cache_write, pack_codes, quantize_nvfp4, quantize_rotated,
                                 quantize_rows, unpack_codes)
 from oracle.codebook import codebook
 from oracle.numformats import bf16_encode
@@ -44,7 +46,10 @@ def test_hand_worked_groups(case):
     else:
         y = np.array([float(v) for v in inputs.split()], np.float32)
     assert y.shape == (16,)
-    enc, sc = quantize_rotated(fmt, y[None, :])
+    if fmt == "nvfp4":
+        enc, sc = quantize_nvfp4(y[None, :])
+    else:
+        enc, sc = quantize_rotated(fmt, y[None, :])
     if fmt == "turbo8":
         got_data = enc[0].tobytes()
         got_scale = sc.astype("<u2").tobytes()
@@ -161,3 +166,39 @@ def test_full_pipeline_mse_report():
         back = wht_f64(dequantize_rows(side, d, s, 128))
         mse = np.mean((back - x) ** 2)
         assert mse < {"turbo2": 0.2, "turbo3": 0.06, "turbo4": 0.02, "turbo8": 0.002}[side]
+
+
+def test_turbo4_beats_nvfp4_mse():
+    """KvCacheDtype::Turbo4's doc claims ~2x lower MSE than NVFP4 at the same
+    bit rate.  With the readings here (NVFP4 scale amax/6, Turbo4 scale
+    amax/c_max after the WHT) the ratio on N(0,1) rows, with and without
+    outlier channels, is ~1.55: Turbo4 is better, by less than the page's
+    round number.  Pinned: the direction and a band around the measured ratio."""
+    from oracle.decode import dequantize_rows
+    from oracle.cache_write import encode_rows_bytes
+    from oracle.wht import wht_f64
+    rng = np.random.default_rng(5)
+    gauss = rng.standard_normal((4096, 128)).astype(np.float32)
+    out = (gauss * np.where(rng.random(128) < 0.02, 10.0, 1.0)).astype(np.float32)
+    for x in (gauss, out):
+        mse = {}
+        for side in ("turbo4", "nvfp4"):
+            d, sc = encode_rows_bytes(side, x)
+            back = dequantize_rows(side, d, sc, 128)
+            if side == "turbo4":
+                back = wht_f64(back)
+            mse[side] = np.mean((back - x) ** 2) / np.mean(x.astype(np.float64) ** 2)
+        ratio = mse["nvfp4"] / mse["turbo4"]
+        assert 1.3 < ratio < 2.5, ratio
+
+
+def test_nvfp4_is_not_rotated_and_dequantizes_to_e2m1_grid():
+    """NVFP4 stores x itself (is_wht_rotated lists the Turbo sides only): a
+    row whose groups are already on the E2M1 grid times a power of two comes
+    back exactly."""
+    from oracle.decode import dequantize_rows
+    from oracle.cache_write import encode_rows_bytes
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -6, -4, -3, -2, -1.5, -1, -0.5, 0], np.float32)
+    x = np.concatenate([grid * 0.25, grid * 8.0])[None, :]
+    d, sc = encode_rows_bytes("nvfp4", x)
+    assert np.array_equal(dequantize_rows("nvfp4", d, sc, 32), x.astype(np.float64))
