@@ -80,8 +80,7 @@ typedef enum kvq_status {
 
 /* Combined cache formats, in the order of [ATLAS] enum KvCacheDtype.
  * kv_pair: the symmetric formats store the same side format in both pools;
- * the asymmetric ones name (K side, V side). NVFP4 is catalogued for
- * sizing only: write/decode reject it with KVQ_ERR_FORMAT. */
+ * the asymmetric ones name (K side, V side). */
 typedef enum kvq_format {
     KVQ_FMT_BF16 = 0,
     KVQ_FMT_FP8 = 1,
@@ -161,8 +160,11 @@ const char* kvq_last_error(void);
  * h = 1, 2, 4, ..., then one multiply by 1/sqrt(head_dim)), take per group
  * of 16 the scale E4M3(amax / max_level) (Turbo8: BF16(amax / 448)), and
  * store code = #{thresholds <= y / scale}; a zero scale stores code 2^(b-1)
- * (Turbo8: byte 0).  FP8 sides store E4M3(x / k_scale) (v_scale).  All
- * E4M3/BF16 encodes round to nearest even and saturate.
+ * (Turbo8: byte 0).  FP8 sides store E4M3(x / k_scale) (v_scale).  NVFP4
+ * ([ATLAS] Nvfp4, "E2M1 packed nibbles", Turbo4's layout) is not rotated:
+ * scale E4M3(amax / 6) per group of 16, code = E2M1(x / scale) (sign bit 3),
+ * a zero scale stores code 0.  All E4M3/BF16/E2M1 encodes round to nearest
+ * even and saturate.
  *
  *   key, value       device, in_dtype elements; row (t,h) as above
  *   k_cache, v_cache device, 16-byte aligned pools

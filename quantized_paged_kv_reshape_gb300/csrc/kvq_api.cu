@@ -122,6 +122,8 @@ const Codebooks& codebooks() {
     fill(4, g_cb.lv4, g_cb.th4);
     fill(3, g_cb.lv3, g_cb.th3);
     fill(2, g_cb.lv2, g_cb.th2);
+    static const float e2m1_mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+    for (int c2 = 0; c2 < 16; ++c2) g_cb.e2m1[c2] = (c2 & 8) ? -e2m1_mag[c2 & 7] : e2m1_mag[c2 & 7];
   });
   return g_cb;
 }
@@ -260,7 +262,6 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
                            int32_t* error_flag, void* stream) {
   if (!fmt_ok(fmt)) return fail(KVQ_ERR_FORMAT, "format %d out of range", (int)fmt);
   const int ks = side_of(fmt, 0), vs = side_of(fmt, 1);
-  if (ks == S_NVFP4 || vs == S_NVFP4) return fail(KVQ_ERR_FORMAT, "nvfp4 has no write kernel");
   if (in_dtype != KVQ_DTYPE_F32 && in_dtype != KVQ_DTYPE_BF16)
     return fail(KVQ_ERR_FORMAT, "in_dtype must be f32 or bf16");
   if (num_tokens < 0 || num_blocks < 0) return fail(KVQ_ERR_ARG, "negative count");
@@ -336,7 +337,6 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
                             int32_t* error_flag, void* stream) {
   if (!fmt_ok(fmt)) return fail(KVQ_ERR_FORMAT, "format %d out of range", (int)fmt);
   const int ks = side_of(fmt, 0), vs = side_of(fmt, 1);
-  if (ks == S_NVFP4 || vs == S_NVFP4) return fail(KVQ_ERR_FORMAT, "nvfp4 has no decode kernel");
   if ((q_dtype != KVQ_DTYPE_F32 && q_dtype != KVQ_DTYPE_BF16) ||
       (out_dtype != KVQ_DTYPE_F32 && out_dtype != KVQ_DTYPE_BF16))
     return fail(KVQ_ERR_FORMAT, "q/out dtype must be f32 or bf16");

@@ -33,20 +33,36 @@ __host__ __device__ constexpr int side_scale_bytes(int s) {
 __host__ __device__ constexpr bool side_rotated(int s) {
   return s == S_T4 || s == S_T3 || s == S_T2 || s == S_T8;
 }
+// Sides whose elements are codes into a level table (Turbo2/3/4: Lloyd-Max
+// levels; NVFP4: the 16 E2M1 values) times a per-16 E4M3 scale.
 __host__ __device__ constexpr bool side_codebook(int s) {
-  return s == S_T4 || s == S_T3 || s == S_T2;
+  return s == S_T4 || s == S_T3 || s == S_T2 || s == S_NVFP4;
 }
 __host__ __device__ constexpr int code_bits(int s) {
-  return s == S_T4 ? 4 : s == S_T3 ? 3 : s == S_T2 ? 2 : 0;
+  return s == S_T4 || s == S_NVFP4 ? 4 : s == S_T3 ? 3 : s == S_T2 ? 2 : 0;
 }
 
 // Lloyd-Max N(0,1) codebooks (fp32 levels ascending, fp32 midpoint
-// thresholds) for 4, 3 and 2 bits, passed to kernels by value.
+// thresholds) for 4, 3 and 2 bits, and the E2M1 values of the 16 NVFP4 codes
+// (code c: sign bit 3, magnitude 0 0.5 1 1.5 2 3 4 6 for c & 7), passed to
+// kernels by value.
 struct Codebooks {
   float lv4[16], th4[15];
   float lv3[8], th3[7];
   float lv2[4], th2[3];
+  float e2m1[16];
 };
+
+// E2M1 code of v: round to nearest, ties to the even code, saturating at 6,
+// sign bit 3 from the sign bit of v.  The magnitude code counts the midpoints
+// below |v|; a midpoint itself goes up only where the code above is even.
+__device__ __forceinline__ uint32_t e2m1_from_float(float v) {
+  const float m = fabsf(v);
+  const uint32_t c = (uint32_t)(m > 0.25f) + (uint32_t)(m >= 0.75f) + (uint32_t)(m > 1.25f) +
+                     (uint32_t)(m >= 1.75f) + (uint32_t)(m > 2.5f) + (uint32_t)(m >= 3.5f) +
+                     (uint32_t)(m > 5.0f);
+  return c | (signbit(v) ? 8u : 0u);
+}
 
 // ------------------------------------------------------- number formats
 

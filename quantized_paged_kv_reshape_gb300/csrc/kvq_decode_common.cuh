@@ -40,7 +40,7 @@ __device__ __forceinline__ void cp_async_wait() {
 
 template <int S>
 __device__ __forceinline__ const float* side_levels(const Codebooks& cb) {
-  return S == S_T4 ? cb.lv4 : S == S_T3 ? cb.lv3 : cb.lv2;
+  return S == S_T4 ? cb.lv4 : S == S_T3 ? cb.lv3 : S == S_NVFP4 ? cb.e2m1 : cb.lv2;
 }
 
 }  // namespace kvq

@@ -148,13 +148,13 @@ struct TcSide {
   static constexpr int KRS =
       S == S_BF16 ? ROW + 16
       : S == S_FP8 ? (ROW % 128 == 0 ? ROW + 64 : ROW)
-      : S == S_T8 || S == S_T4 ? ROW + 16
+      : S == S_T8 || S == S_T4 || S == S_NVFP4 ? ROW + 16
       : S == S_T3 ? (HD == 256 ? ROW + 16 : ROW)
       : /* T2 */ (HD == 64 ? ROW : ROW + 16);
   static constexpr int VRS =
       S == S_BF16 ? ROW + 16
       : S == S_FP8 ? (HD == 64 ? 80 : HD == 128 ? 144 : ROW + 16)
-      : S == S_T8 || S == S_T4 ? ROW + 16
+      : S == S_T8 || S == S_T4 || S == S_NVFP4 ? ROW + 16
       : S == S_T3 ? (HD == 256 ? ROW + 16 : ROW)
       : /* T2 */ (HD == 64 ? ROW : ROW + 16);
   static constexpr int LUT_BYTES = CB ? (1 << (2 * code_bits(S))) * 16 * 8 : 0;
@@ -193,7 +193,7 @@ struct TcCfg {
   static constexpr int OFF_V = OFF_KS + SLAB * K::SROW;
   static constexpr int OFF_VS = OFF_V + SLAB * V::VRS;
   static constexpr int STAGE = (OFF_VS + SLAB * V::SROW + 15) / 16 * 16;
-  static constexpr bool SHARE_LUT = K::CB && V::CB && code_bits(KS) == code_bits(VS);
+  static constexpr bool SHARE_LUT = K::CB && V::CB && KS == VS;
   static constexpr int LUTS = K::LUT_BYTES + (SHARE_LUT ? 0 : V::LUT_BYTES);
   static constexpr int MAXP = 512;                             // pages staged per stretch
   static constexpr int OFF_BLK = 8 * HD * 4;                   // after q_s [8][HD] fp32

@@ -28,6 +28,7 @@ bool decode_tc_supported(int k_side, int v_side) {
     case S_T3: return v_side == S_T3 || v_side == S_T8;
     case S_T2: return v_side == S_T2;
     case S_T8: return v_side == S_T8;
+    case S_NVFP4: return v_side == S_NVFP4;
     default: return false;
   }
 }
@@ -41,6 +42,7 @@ cudaError_t launch_decode_tc(int k_side, int v_side, int hd, const DecodeArgs& a
     case S_T3: return launch_tc_k_t3(v_side, hd, a, cb, st);
     case S_T2: return launch_tc_k_t2(v_side, hd, a, cb, st);
     case S_T8: return launch_tc_k_t8(v_side, hd, a, cb, st);
+    case S_NVFP4: return launch_tc_k_nvfp4(v_side, hd, a, cb, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -73,5 +73,6 @@ cudaError_t launch_tc_k_t4(int v_side, int hd, const DecodeArgs&, const Codebook
 cudaError_t launch_tc_k_t3(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 cudaError_t launch_tc_k_t2(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 cudaError_t launch_tc_k_t8(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tc_k_nvfp4(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 
 }  // namespace kvq

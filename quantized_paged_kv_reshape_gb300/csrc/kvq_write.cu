@@ -134,6 +134,23 @@ __device__ __forceinline__ void write_turbo(float (&y)[HD / 32], const float lv_
   if ((lane % LPG) == 0) row_scales[lane / LPG] = sbyte;
 }
 
+// NVFP4: per 16-element group s = E4M3(amax / 6), code = E2M1(x / s) (both
+// fp32 divides); a zero scale stores code 0.  No rotation.
+template <int HD>
+__device__ __forceinline__ void write_nvfp4(const float (&x)[HD / 32], uint8_t* row_codes,
+                                            uint8_t* row_scales, int lane) {
+  constexpr int E = HD / 32;
+  const float amax = group_amax<E>(x);
+  const uint8_t sbyte = e4m3_from_float(amax / 6.0f);
+  const float s = e4m3_to_float(sbyte);
+  int code[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) code[i] = s == 0.f ? 0 : (int)e2m1_from_float(x[i] / s);
+  store_codes<4, E>(row_codes, code, lane);
+  constexpr int LPG = kGroup / E;
+  if ((lane % LPG) == 0) row_scales[lane / LPG] = sbyte;
+}
+
 // Encode and store one row already loaded into x (lane's E elements).
 template <int HD>
 __device__ __forceinline__ void write_row(const WriteArgs& a, const Codebooks& cb, int side, int64_t slot,
@@ -175,6 +192,8 @@ __device__ __forceinline__ void write_row(const WriteArgs& a, const Codebooks& c
     if constexpr (E == 2) store_bytes<2>(dst, w[0]);
     else if constexpr (E == 4) store_bytes<4>(dst, w[0]);
     else store_bytes<8>(dst, w[0], w[1]);
+  } else if (fmt == S_NVFP4) {
+    write_nvfp4<HD>(x, base + ridx * (HD / 2), base + dsec + ridx * (HD / kGroup), lane);
   } else {
     fwht_warp<E>(x, lane, a.inv_sqrt_hd);
     if (fmt == S_T8) {

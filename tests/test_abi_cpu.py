@@ -87,7 +87,6 @@ def _write(**over):
 def test_write_rejects_bad_arguments():
     assert _write(key=None) == A.KVQ_ERR_ARG
     assert _write(head_dim=96) == A.KVQ_ERR_SHAPE
-    assert _write(fmt=2) == A.KVQ_ERR_FORMAT            # nvfp4: sizing only
     assert _write(fmt=42) == A.KVQ_ERR_FORMAT
     assert _write(in_dtype=7) == A.KVQ_ERR_FORMAT
     assert _write(k_block_stride_bytes=4096) == A.KVQ_ERR_ARG  # below block bytes
@@ -120,7 +119,6 @@ def test_decode_rejects_bad_arguments():
     assert _decode(workspace_bytes=16) == A.KVQ_ERR_WORKSPACE
     assert _decode(workspace=None) == A.KVQ_ERR_ARG
     assert _decode(workspace=8200) == A.KVQ_ERR_ALIGN
-    assert _decode(fmt=2) == A.KVQ_ERR_FORMAT
     assert _decode(sparse_v_threshold=-1.0) == A.KVQ_ERR_ARG
     assert _decode(q_stride=100) == A.KVQ_ERR_ARG
     assert _decode(fmt=15, k_scale=-1.0) == A.KVQ_ERR_ARG
