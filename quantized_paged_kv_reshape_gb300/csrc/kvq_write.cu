@@ -112,22 +112,19 @@ __device__ __forceinline__ float group_amax(const float (&y)[E]) {
 
 template <int HD, int B>
 __device__ __forceinline__ void write_turbo(float (&y)[HD / 32], const float lv_max,
-                                            const float (&th)[(1 << B) - 1], uint8_t* row_codes,
-                                            uint8_t* row_scales, int lane) {
+                                            const uint2* bucket, const float* th2,
+                                            uint8_t* row_codes, uint8_t* row_scales, int lane) {
   constexpr int E = HD / 32;
   const float amax = group_amax<E>(y);
   const float ratio = amax / lv_max;               // IEEE fp32 divide
   const uint8_t sbyte = e4m3_from_float(ratio);
   const float s = e4m3_to_float(sbyte);
+  const float r = s == 0.f ? 0.f : 1.f / s;
   int code[E];
 #pragma unroll
-  for (int i = 0; i < E; ++i) {
-    if (s == 0.f) {
-      code[i] = 1 << (B - 1);
-    } else {
-      const float v = y[i] / s;                     // IEEE fp32 divide
-      code[i] = B == 4 ? lm_code4(v, th) : B == 3 ? lm_code3(v, th) : lm_code2(v, th);
-    }
+  for (int i = 0; i < E; ++i) {  // v = y / s, IEEE-rounded
+    const float v = div_by_scale(y[i], s, r);
+    code[i] = s == 0.f ? 1 << (B - 1) : B == 2 ? lm_code2(v, th2) : lm_code_bucket<B>(v, bucket);
   }
   store_codes<B, E>(row_codes, code, lane);
   constexpr int LPG = kGroup / E;
@@ -143,9 +140,11 @@ __device__ __forceinline__ void write_nvfp4(const float (&x)[HD / 32], uint8_t* 
   const float amax = group_amax<E>(x);
   const uint8_t sbyte = e4m3_from_float(amax / 6.0f);
   const float s = e4m3_to_float(sbyte);
+  const float r = s == 0.f ? 0.f : 1.f / s;
   int code[E];
 #pragma unroll
-  for (int i = 0; i < E; ++i) code[i] = s == 0.f ? 0 : (int)e2m1_from_float(x[i] / s);
+  for (int i = 0; i < E; ++i)   // x / s IEEE-rounded; its sign is that of x
+    code[i] = s == 0.f ? 0 : (int)e2m1_from_float(div_by_scale(x[i], s, r), signbit(x[i]));
   store_codes<4, E>(row_codes, code, lane);
   constexpr int LPG = kGroup / E;
   if ((lane % LPG) == 0) row_scales[lane / LPG] = sbyte;
@@ -153,7 +152,8 @@ __device__ __forceinline__ void write_nvfp4(const float (&x)[HD / 32], uint8_t* 
 
 // Encode and store one row already loaded into x (lane's E elements).
 template <int HD>
-__device__ __forceinline__ void write_row(const WriteArgs& a, const Codebooks& cb, int side, int64_t slot,
+__device__ __forceinline__ void write_row(const WriteArgs& a, const Codebooks& cb,
+                                          const uint2 (*bucket)[kBuckets], int side, int64_t slot,
                                           int h, float (&x)[HD / 32], int lane) {
   constexpr int E = HD / 32;
   int64_t blk;
@@ -214,22 +214,16 @@ __device__ __forceinline__ void write_row(const WriteArgs& a, const Codebooks& c
       if ((lane % LPG) == 0)
         store_bytes<2>(base + dsec + (ridx * (HD / kGroup) + lane / LPG) * 2, sbits);
     } else if (fmt == S_T4) {
-      float th[15];
-#pragma unroll
-      for (int i = 0; i < 15; ++i) th[i] = cb.th4[i];
-      write_turbo<HD, 4>(x, cb.lv4[15], th, base + ridx * (HD / 2),
+      write_turbo<HD, 4>(x, cb.lv4[15], bucket[0], nullptr, base + ridx * (HD / 2),
                          base + dsec + ridx * (HD / kGroup), lane);
     } else if (fmt == S_T3) {
-      float th[7];
-#pragma unroll
-      for (int i = 0; i < 7; ++i) th[i] = cb.th3[i];
-      write_turbo<HD, 3>(x, cb.lv3[7], th, base + ridx * (HD * 3 / 8),
+      write_turbo<HD, 3>(x, cb.lv3[7], bucket[1], nullptr, base + ridx * (HD * 3 / 8),
                          base + dsec + ridx * (HD / kGroup), lane);
     } else {
       float th[3];
 #pragma unroll
       for (int i = 0; i < 3; ++i) th[i] = cb.th2[i];
-      write_turbo<HD, 2>(x, cb.lv2[3], th, base + ridx * (HD / 4),
+      write_turbo<HD, 2>(x, cb.lv2[3], bucket[2], th, base + ridx * (HD / 4),
                          base + dsec + ridx * (HD / kGroup), lane);
     }
   }
@@ -243,8 +237,13 @@ template <int HD, typename InT, bool VEC>
 __global__ void __launch_bounds__(256)
 cache_write_kernel(const WriteArgs a, const Codebooks cb) {
   constexpr int E = HD / 32;
-  constexpr int RB = HD == 256 ? 2 : 4;
+  constexpr int RB = 2;  // measured on GB300: 2 beats 1 and 4 for every format
   const int lane = threadIdx.x & 31;
+  __shared__ uint2 bucket[3][kBuckets];  // codebook-search buckets (4, 3, 2 bits)
+  for (int i = threadIdx.x; i < 3 * kBuckets; i += blockDim.x)
+    bucket[i / kBuckets][i % kBuckets] =
+        make_uint2(cb.bucket[i / kBuckets][i % kBuckets][0], cb.bucket[i / kBuckets][i % kBuckets][1]);
+  __syncthreads();
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t rows = (int64_t)a.num_tokens * a.nkv * 2;
   for (int64_t row0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RB;
@@ -282,7 +281,7 @@ cache_write_kernel(const WriteArgs a, const Codebooks cb) {
     }
 #pragma unroll
     for (int r = 0; r < RB; ++r)
-      if (slot[r] >= 0) write_row<HD>(a, cb, side[r], slot[r], head[r], x[r], lane);
+      if (slot[r] >= 0) write_row<HD>(a, cb, bucket, side[r], slot[r], head[r], x[r], lane);
   }
 }
 

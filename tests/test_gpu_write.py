@@ -87,3 +87,59 @@ def test_write_empty_is_noop():
                     "turbo4", 2, 128, 16)
     torch.cuda.synchronize()
     assert not kpool.any()
+
+
+def _near_threshold_rows(side, hd, rng):
+    """Rows whose quantizer inputs y sit within a few ulps of a decision
+    boundary times the group scale: element 0 of every group fixes the scale
+    (amax = largest level x s, s an E4M3 value), the others are a boundary x s
+    nudged by -3..3 ulps.  Boundaries: the Lloyd-Max midpoint thresholds, or
+    the E2M1 midpoints for nvfp4."""
+    if side == "nvfp4":
+        bounds, top = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32), 6.0
+    else:
+        bits = oracle.formats.CODE_BITS[side]
+        _, lv32, thr = oracle.codebook(bits)
+        bounds, top = thr.astype(np.float32), float(lv32[-1])
+    scales = oracle.e4m3_decode(np.arange(0x08, 0x7E, dtype=np.uint8)).astype(np.float32)
+    n_groups = 512
+    y = np.zeros((n_groups, 16), np.float32)
+    for g in range(n_groups):
+        s = scales[rng.integers(len(scales))]
+        y[g, 0] = np.float32(top) * s
+        b = bounds[rng.integers(len(bounds), size=15)]
+        v = (b * s).astype(np.float32)
+        steps = rng.integers(-3, 4, size=15)
+        for i in range(15):
+            for _ in range(abs(steps[i])):
+                v[i] = np.nextafter(v[i], np.float32(np.inf if steps[i] > 0 else -np.inf))
+        y[g, 1:] = v * rng.choice(np.array([-1, 1], np.float32), 15)
+    y = y.reshape(-1, hd)
+    # Rotated sides quantize WHT(x): feed x = WHT(y) (fp32, self-inverse up to
+    # rounding), so the kernel's rotated values land within a few ulps of y.
+    return y if side == "nvfp4" else oracle.fwht_f32(y)
+
+
+@pytest.mark.parametrize("fmt", ["turbo4", "turbo3", "turbo2", "nvfp4"])
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_write_near_decision_boundaries(fmt, hd):
+    """Codes of values a few ulps from a threshold: the kernel's quotient and
+    code search must round exactly like the oracle's fp32 division."""
+    rng = np.random.default_rng(hd)
+    nkv, bs = 2, 16
+    x = _near_threshold_rows(fmt, hd, rng).astype(np.float32)
+    ntok = x.shape[0] // nkv
+    x = x[: ntok * nkv].reshape(ntok, nkv, hd)
+    num_blocks = -(-ntok // bs)
+    slots = np.arange(ntok, dtype=np.int64)
+    st = (oracle.block_bytes(fmt, bs, nkv, hd) + 15) // 16 * 16
+    kc = np.zeros(num_blocks * st, np.uint8)
+    oracle.cache_write(fmt, x, kc, slots, nkv, hd, bs, st)
+    xd = torch.from_numpy(x).cuda()
+    kpool = torch.zeros((num_blocks, st), dtype=torch.uint8, device="cuda")
+    vpool = torch.zeros((num_blocks, st), dtype=torch.uint8, device="cuda")
+    ops.cache_write(xd.view(ntok, -1), xd.view(ntok, -1), kpool, vpool,
+                    torch.from_numpy(slots).cuda(), fmt, nkv, hd, bs)
+    torch.cuda.synchronize()
+    got = kpool.cpu().numpy().reshape(-1)
+    assert np.array_equal(got, kc), f"{int((got != kc).sum())} bytes differ"
