@@ -122,6 +122,24 @@ def dist_info():
     return ws, rank, local
 
 
+def slowest_rank(values, dev):
+    """Each value maxed over the ranks of the job (the job is as slow as its
+    slowest rank); unchanged on one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_rate(bytes_per_rank_step, world_size, ms_per_step):
+    """Whole-job throughput in GB/s: every rank processes its own units (weak
+    scaling), the step lasts as long as the slowest rank."""
+    return bytes_per_rank_step * world_size / (ms_per_step * 1e-3) / 1e9
+
+
 def algorithmic_decode_bytes(fmt, seq_lens, nkv, hd, bs, window=0):
     from quantized_paged_kv_reshape_gb300 import ops
     per_tok = 0
@@ -315,11 +333,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1) / e_steps
 
-    ms_step = ms_total / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_step, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, e2e_ms = float(t[0]), float(t[1])
+    ms_step, e2e_ms = slowest_rank([ms_total / args.steps, e2e_ms], dev)
 
     dec_bytes = {(f, win): algorithmic_decode_bytes(f, w.seq_lens, nkv, hd, bs, win)
                  for f in fmts for win in windows}
@@ -343,8 +357,8 @@ def run_gpu(args):
                         "step_write_us": round(us_w, 2), "step_write_tokens": wtok,
                         "step_write_gbs": round(write_bytes(f, wtok, nkv, hd, bs, in_bytes) / (us_w * 1e-6) / 1e9, 1)}
     dom = max(per_layer, key=lambda k: per_layer[k]["us_per_layer"])
-    value = step_bytes * ws / (ms_step * 1e-3) / 1e9
-    e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
+    value = job_rate(step_bytes, ws, ms_step)
+    e2e_value = job_rate(step_bytes, ws, e2e_ms)
     launches_per_step = len(fmts) * ((2 if prefill is not None else 1) + len(windows))
     dom_fmt = dom.split("@")[0]
     traffic = TRAFFIC.get((args.workload, dom)) if not args.num_seqs or args.num_seqs == W.make(args.workload).num_seqs else None
