@@ -16,7 +16,8 @@ Source pages (cited in each module by page title and section):
   ``[num_blocks, block_size, num_kv_heads, head_dim]`` layout, code section
   then scale section, launcher arguments of the write and decode kernels.
 * "combs_models/kv.rs" (burn): ``attend`` (scores -> softmax -> P.V with the
-  ``repeat_kv`` GQA mapping) and the paged slot arithmetic.
+  ``repeat_kv`` GQA mapping, causal for several query rows) and the paged
+  slot arithmetic.
 
 Parity status per function (what pins it) is listed in each module header.
 """
@@ -35,3 +36,4 @@ from .cache_write import (  # noqa: F401
     cache_write,
 )
 from .decode import dequantize_rows, gather_side, paged_decode  # noqa: F401
+from .prefill import paged_prefill  # noqa: F401
