@@ -249,6 +249,43 @@ kvq_status kvq_paged_decode(
     void* workspace, size_t workspace_bytes, kvq_format fmt,
     int32_t* error_flag, void* stream);
 
+/* ---------------------------------------------------------- chunked prefill */
+
+/* [BURN] attend with its causal mask for several query rows + repeat_kv;
+ * [ATLAS] is_wht_rotated bookends.  Attention of a chunk of new query tokens
+ * per sequence over the quantized paged cache, after the chunk's K/V rows
+ * were written (kvq_cache_write).  The pages name chunked prefill over the
+ * quantized cache as the step after the write; the semantics are read as:
+ * sequence s holds L = seq_lens[s] positions, its C = cu_q[s+1] - cu_q[s]
+ * queries (rows cu_q[s] .. cu_q[s+1]-1 of q) are the last C positions, and
+ * query i at p = L - C + i attends to the positions [lo, p], lo = max(0,
+ * p + 1 - sliding_window) (lo = 0 when sliding_window == 0):
+ *   out[row, j, :] = sum_t softmax_t(sm_scale * q[row,j].k_t) v_t
+ * over those positions, with kv head j / (num_q_heads/num_kv_heads).  A query
+ * with p < 0 (C > L) gives a zero row.
+ *
+ *   q            device, q_dtype, row (r, j) at element r*q_stride + j*head_dim
+ *   cu_q         device int32 [num_seqs + 1], cu_q[0] = 0, non-decreasing
+ *   max_chunk    host: an upper bound of every C (sizes the launch; queries
+ *                beyond it are not computed)
+ *   out          device, out_dtype, contiguous [cu_q[num_seqs], num_q_heads, head_dim]
+ *   other arguments as kvq_paged_decode (no workspace; no sparse-V skip).
+ * One kernel launch: a CTA per (tile of query rows, kv head, sequence); the
+ * contraction runs on tensor cores. */
+kvq_status kvq_paged_prefill(
+    const void* q, kvq_dtype q_dtype, int64_t q_stride,
+    const int32_t* cu_q, int32_t max_chunk,
+    const void* k_cache, const void* v_cache,
+    void* out, kvq_dtype out_dtype,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens, int32_t num_seqs, int64_t num_blocks,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size,
+    int64_t k_block_stride_bytes, int64_t v_block_stride_bytes,
+    float sm_scale, float k_scale, float v_scale,
+    int32_t sliding_window, kvq_format fmt,
+    int32_t* error_flag, void* stream);
+
 /* -------------------------------------------- decode without an allocation */
 
 /* Bytes of the scratch array built into the library for

@@ -63,6 +63,11 @@ _SIGS = {
         C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_int64, C.c_int32, C.c_int32,
         C.c_int32, C.c_int32, C.c_int64, C.c_int64, C.c_float, C.c_float, C.c_float,
         C.c_int32, C.c_float, C.c_int, C.c_void_p, C.c_void_p]),
+    "kvq_paged_prefill": (C.c_int, [
+        C.c_void_p, C.c_int, C.c_int64, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
+        C.c_void_p, C.c_int, C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_int64,
+        C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_int64, C.c_float,
+        C.c_float, C.c_float, C.c_int32, C.c_int, C.c_void_p, C.c_void_p]),
 }
 
 KVQ_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -166,10 +171,23 @@ def kvq_paged_decode_noalloc(q, q_dtype, q_stride, k_cache, v_cache, out, out_dt
                              v_scale, sliding_window, sparse_v_threshold, fmt, error_flag,
                              stream):
     """Decode without a workspace argument, for callers that cannot allocate
-    device memory: the split-K partials use a fixed 8 MiB scratch array built
-    into the library (shared by all calls; overlapping calls race)."""
+    device memory: the partials and merge counters use a fixed 8 MiB scratch
+    array built into the library (shared by all calls; overlapping calls race)."""
     check(lib().kvq_paged_decode_noalloc(
         q, q_dtype, q_stride, k_cache, v_cache, out, out_dtype, block_tables,
         max_blocks_per_seq, seq_lens, num_seqs, num_blocks, num_q_heads, num_kv_heads,
         head_dim, block_size, k_block_stride_bytes, v_block_stride_bytes, sm_scale, k_scale,
         v_scale, sliding_window, sparse_v_threshold, int(fmt), error_flag, stream))
+
+
+def kvq_paged_prefill(q, q_dtype, q_stride, cu_q, max_chunk, k_cache, v_cache, out, out_dtype,
+                      block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_blocks,
+                      num_q_heads, num_kv_heads, head_dim, block_size, k_block_stride_bytes,
+                      v_block_stride_bytes, sm_scale, k_scale, v_scale, sliding_window, fmt,
+                      error_flag, stream):
+    """Raw call with integer device addresses; raises KvqError on a bad status."""
+    check(lib().kvq_paged_prefill(
+        q, q_dtype, q_stride, cu_q, max_chunk, k_cache, v_cache, out, out_dtype, block_tables,
+        max_blocks_per_seq, seq_lens, num_seqs, num_blocks, num_q_heads, num_kv_heads,
+        head_dim, block_size, k_block_stride_bytes, v_block_stride_bytes, sm_scale, k_scale,
+        v_scale, sliding_window, int(fmt), error_flag, stream))

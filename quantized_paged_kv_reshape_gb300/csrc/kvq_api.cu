@@ -433,4 +433,83 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   return ok();
 }
 
+kvq_status kvq_paged_prefill(const void* q, kvq_dtype q_dtype, int64_t q_stride, const int32_t* cu_q,
+                             int32_t max_chunk, const void* k_cache, const void* v_cache, void* out,
+                             kvq_dtype out_dtype, const int32_t* block_tables, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t num_seqs, int64_t num_blocks, int32_t nq,
+                             int32_t nkv, int32_t hd, int32_t bs, int64_t k_bstride, int64_t v_bstride,
+                             float sm_scale, float k_scale, float v_scale, int32_t window,
+                             kvq_format fmt, int32_t* error_flag, void* stream) {
+  if (!fmt_ok(fmt)) return fail(KVQ_ERR_FORMAT, "format %d out of range", (int)fmt);
+  const int ks = side_of(fmt, 0), vs = side_of(fmt, 1);
+  if ((q_dtype != KVQ_DTYPE_F32 && q_dtype != KVQ_DTYPE_BF16) ||
+      (out_dtype != KVQ_DTYPE_F32 && out_dtype != KVQ_DTYPE_BF16))
+    return fail(KVQ_ERR_FORMAT, "q/out dtype must be f32 or bf16");
+  if (hd != 64 && hd != 128 && hd != 256) return fail(KVQ_ERR_SHAPE, "head_dim %d not in {64,128,256}", hd);
+  if (bs != 8 && bs != 16 && bs != 32) return fail(KVQ_ERR_SHAPE, "block_size %d not in {8,16,32}", bs);
+  if (nkv < 1 || nq < 1 || nq % nkv) return fail(KVQ_ERR_SHAPE, "num_q_heads must be a multiple of num_kv_heads");
+  const int rep = nq / nkv;
+  const int rp = rmax_for(rep);
+  if (!rp) return fail(KVQ_ERR_SHAPE, "grouped-query ratio %d above 8", rep);
+  if (num_seqs < 0 || num_blocks < 0 || window < 0 || max_chunk < 0) return fail(KVQ_ERR_ARG, "negative count");
+  if (!std::isfinite(sm_scale)) return fail(KVQ_ERR_ARG, "sm_scale must be finite");
+  if (num_seqs == 0 || max_chunk == 0) return ok();
+  if (max_blocks < 1) return fail(KVQ_ERR_ARG, "max_blocks_per_seq must be >= 1");
+  if (!q || !cu_q || !k_cache || !v_cache || !out || !block_tables || !seq_lens)
+    return fail(KVQ_ERR_ARG, "null pointer");
+  if (q_stride < (int64_t)nq * hd) return fail(KVQ_ERR_ARG, "q_stride smaller than num_q_heads*head_dim");
+  const int64_t kb = kvq_block_bytes(fmt, 0, bs, nkv, hd), vb = kvq_block_bytes(fmt, 1, bs, nkv, hd);
+  if (k_bstride < kb || v_bstride < vb) return fail(KVQ_ERR_ARG, "block stride below block bytes");
+  if (k_bstride % 16 || v_bstride % 16 || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(KVQ_ERR_ALIGN, "caches and block strides must be 16-byte aligned");
+  if ((ks == S_FP8 && !(k_scale > 0.f && std::isfinite(k_scale))) ||
+      (vs == S_FP8 && !(v_scale > 0.f && std::isfinite(v_scale))))
+    return fail(KVQ_ERR_ARG, "FP8 side needs a finite scale > 0");
+  if (!decode_tc_supported(ks, vs)) return fail(KVQ_ERR_FORMAT, "no prefill instance for this pair");
+  const Codebooks& cb = codebooks();
+  const double scale = sm_scale == 0.f ? 1.0 / std::sqrt((double)hd) : (double)sm_scale;
+  PrefillArgs a{};
+  a.q = q;
+  a.q_stride = q_stride;
+  a.q_bf16 = q_dtype == KVQ_DTYPE_BF16;
+  a.cu_q = cu_q;
+  a.k_cache = (const uint8_t*)k_cache;
+  a.v_cache = (const uint8_t*)v_cache;
+  a.out = out;
+  a.out_bf16 = out_dtype == KVQ_DTYPE_BF16;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs;
+  a.num_blocks = num_blocks;
+  a.nq = nq;
+  a.nkv = nkv;
+  a.rep = rep;
+  a.rp = rp;
+  a.bs = bs;
+  a.k_bstride = k_bstride;
+  a.v_bstride = v_bstride;
+  a.k_dsec = kvq_data_section_bytes(fmt, 0, bs, nkv, hd);
+  a.v_dsec = kvq_data_section_bytes(fmt, 1, bs, nkv, hd);
+  a.score_scale = (float)(scale * M_LOG2E * (ks == S_FP8 ? (double)k_scale : 1.0));
+  a.v_mult = vs == S_FP8 ? v_scale : 1.0f;
+  a.inv_sqrt_hd = (float)(1.0 / std::sqrt((double)hd));
+  a.window = window;
+  a.err = error_flag;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e;
+  switch (ks) {
+    case S_BF16: e = launch_pf_k_bf16(vs, hd, a, cb, max_chunk, st); break;
+    case S_FP8: e = launch_pf_k_fp8(vs, hd, a, cb, max_chunk, st); break;
+    case S_T4: e = launch_pf_k_t4(vs, hd, a, cb, max_chunk, st); break;
+    case S_T3: e = launch_pf_k_t3(vs, hd, a, cb, max_chunk, st); break;
+    case S_T2: e = launch_pf_k_t2(vs, hd, a, cb, max_chunk, st); break;
+    case S_T8: e = launch_pf_k_t8(vs, hd, a, cb, max_chunk, st); break;
+    case S_NVFP4: e = launch_pf_k_nvfp4(vs, hd, a, cb, max_chunk, st); break;
+    default: e = cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 }  // extern "C"

@@ -60,6 +60,30 @@ struct DecodeArgs {  // arguments of the paged decode (decode_tc_kernel)
 };
 
 
+struct PrefillArgs {  // arguments of the chunked prefill (prefill_tc_kernel)
+  const void* q;
+  int64_t q_stride;          // elements between query tokens
+  int q_bf16;
+  const int32_t* cu_q;       // [num_seqs + 1]
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  void* out;                 // [total_q][nq][hd]
+  int out_bf16;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  int32_t num_seqs;
+  int64_t num_blocks;        // 0 = unchecked
+  int32_t nq, nkv, rep, rp;  // rp = rep rounded up to a power of two
+  int32_t bs;
+  int64_t k_bstride, v_bstride, k_dsec, v_dsec;
+  float score_scale;         // sm_scale * log2(e) (* k_scale for FP8 K)
+  float v_mult;              // v_scale for FP8 V, else 1
+  float inv_sqrt_hd;
+  int32_t window;
+  int32_t* err;
+};
+
 cudaError_t launch_cache_write(const WriteArgs& a, const Codebooks& cb, int head_dim,
                                bool in_bf16, bool vec, int grid, cudaStream_t st);
 
@@ -74,5 +98,14 @@ cudaError_t launch_tc_k_t3(int v_side, int hd, const DecodeArgs&, const Codebook
 cudaError_t launch_tc_k_t2(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 cudaError_t launch_tc_k_t8(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 cudaError_t launch_tc_k_nvfp4(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
+
+// Chunked prefill (kvq_prefill_k_*.cu), same pairs as the decode.
+cudaError_t launch_pf_k_bf16(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);
+cudaError_t launch_pf_k_fp8(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);
+cudaError_t launch_pf_k_t4(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);
+cudaError_t launch_pf_k_t3(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);
+cudaError_t launch_pf_k_t2(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);
+cudaError_t launch_pf_k_t8(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);
+cudaError_t launch_pf_k_nvfp4(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);
 
 }  // namespace kvq

@@ -1,0 +1,19 @@
+// Chunked-prefill instances whose K side is T4 (one translation unit
+// per K side so the instances compile in parallel).  V sides: the
+// catalogue's pairs with this K side ("spark_runtime/kv_cache.rs",
+// KvCacheDtype::kv_pair).
+#include "kvq_prefill.cuh"
+
+namespace kvq {
+
+cudaError_t launch_pf_k_t4(int v_side, int hd, const PrefillArgs& a, const Codebooks& cb,
+                            int max_chunk, cudaStream_t st) {
+  switch (v_side) {
+    case S_T4: return launch_prefill_pair<S_T4, S_T4>(hd, a, cb, max_chunk, st);
+    case S_T3: return launch_prefill_pair<S_T4, S_T3>(hd, a, cb, max_chunk, st);
+    case S_T8: return launch_prefill_pair<S_T4, S_T8>(hd, a, cb, max_chunk, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

@@ -111,3 +111,33 @@ def paged_decode(q, k_cache, v_cache, block_tables, seq_lens, fmt, num_kv_heads,
         workspace.numel() * workspace.element_size(), fmt_id(fmt),
         _dev_ptr(error_flag, "error_flag"), _stream_ptr(stream))
     return out
+
+
+def paged_prefill(q, cu_q, max_chunk, k_cache, v_cache, block_tables, seq_lens, fmt,
+                  num_kv_heads, block_size, out=None, out_dtype=torch.float32, sm_scale=0.0,
+                  k_scale=1.0, v_scale=1.0, sliding_window=0, num_blocks=None, error_flag=None,
+                  stream=None):
+    """Chunked-prefill attention: q [total_q, num_q_heads, head_dim] (row stride
+    q.stride(0)), cu_q int32 [num_seqs + 1] query offsets per sequence, the last
+    cu_q[s+1] - cu_q[s] of sequence s's seq_lens[s] cached positions being its
+    queries (causal)."""
+    total_q, nq, hd = q.shape
+    if q.stride(2) != 1 or q.stride(1) != hd:
+        raise ValueError("q heads must be contiguous [.., num_q_heads, head_dim]")
+    for t, name in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (cu_q, "cu_q")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous int32")
+    num_seqs = seq_lens.shape[0]
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty((total_q, nq, hd), dtype=out_dtype, device=q.device)
+    nb = k_cache.shape[0] if num_blocks is None else num_blocks
+    A.kvq_paged_prefill(
+        _dev_ptr(q, "q"), _dtype_code(q, "q"), q.stride(0), _dev_ptr(cu_q, "cu_q"),
+        int(max_chunk), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+        _dev_ptr(out, "out"), _dtype_code(out, "out"), _dev_ptr(block_tables, "block_tables"),
+        mb, _dev_ptr(seq_lens, "seq_lens"), num_seqs, nb, nq, num_kv_heads, hd, block_size,
+        k_cache.stride(0), v_cache.stride(0), float(sm_scale), float(k_scale), float(v_scale),
+        int(sliding_window), fmt_id(fmt), _dev_ptr(error_flag, "error_flag"),
+        _stream_ptr(stream))
+    return out
