@@ -50,6 +50,8 @@ WORKLOAD_DESC = {
     "gemma_write": "write-heavy step: 8192-token fused-QKV write (stride 16384) + decode over "
                    "{nseq} seqs x 8192, 32 q / 16 kv heads, head_dim 256",
     "tiny": "tiny: {nseq} seqs of 37/50 tokens, 4 q / 2 kv heads, head_dim 64",
+    "prefill": "chunked prefill layer: {nseq} seqs x 4096 ctx, last 512 positions the new chunk "
+               "(written, then attended causally), 32 q / 8 kv heads, head_dim 128, block_size 16",
 }
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # decode launch, from the ncu capture summarised in profiles/ (None when the
@@ -440,6 +442,131 @@ def cpu_baseline(seconds=15.0):
                       "(all cores)"}
 
 
+def prefill_flops(seq_lens, chunk, nq, hd):
+    """Algorithmic FLOPs of one chunked-prefill layer: query i of a chunk of C
+    over L positions attends p + 1 = L - C + i + 1 keys; per key and query
+    head 2*hd for q.k and 2*hd for p.v."""
+    keys = sum(chunk * (int(L) - chunk) + chunk * (chunk + 1) // 2 for L in seq_lens)
+    return 4 * hd * nq * keys
+
+
+def run_prefill(args):
+    """Chunked-prefill leg: per format, the write of every sequence's last
+    `chunk` positions, then their causal attention over the paged cache."""
+    import torch
+    from quantized_paged_kv_reshape_gb300 import ops, workloads as W
+    from quantized_paged_kv_reshape_gb300 import _abi
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    _abi.lib()
+    w = W.make("prefill", seed=rank)
+    nkv, nq, hd, bs, C = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size, w.chunk
+    nseq = w.num_seqs
+    lens_np = np.asarray(w.seq_lens, np.int64)
+    tables_np = W.block_tables(w)
+    tables = torch.from_numpy(tables_np).to(dev)
+    lens = torch.from_numpy(w.seq_lens).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4321 + rank)
+    ntok = int(lens_np.sum())
+    slots_all = torch.from_numpy(W.slot_mapping_for_sequences(w, tables_np)).to(dev)
+    ch_k = torch.from_numpy(W.channel_scales(w, 0)).to(dev)
+    ch_v = torch.from_numpy(W.channel_scales(w, 1)).to(dev)
+    kall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_k).to(torch.bfloat16)
+    vall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_v).to(torch.bfloat16)
+    k_scale = float(kall.float().abs().amax()) / 448.0
+    v_scale = float(vall.float().abs().amax()) / 448.0
+    starts = np.concatenate([[0], np.cumsum(lens_np)])
+    chunk_idx = torch.from_numpy(np.concatenate([np.arange(starts[s + 1] - C, starts[s + 1])
+                                                 for s in range(nseq)])).to(dev)
+    kc, vc, sc = (kall[chunk_idx].contiguous(), vall[chunk_idx].contiguous(),
+                  slots_all[chunk_idx].contiguous())
+    cu = torch.from_numpy(np.arange(0, (nseq + 1) * C, C, dtype=np.int32)).to(dev)
+    q = torch.randn((nseq * C, nq, hd), generator=g, device=dev).to(torch.bfloat16)
+    fmts = args.formats.split(",") if args.formats else list(w.formats)
+    pools, outs = {}, {}
+    for f in fmts:
+        kp = ops.alloc_pool(w.num_blocks, f, 0, bs, nkv, hd, device=dev)
+        vp = ops.alloc_pool(w.num_blocks, f, 1, bs, nkv, hd, device=dev)
+        ops.cache_write(kall.view(ntok, -1), vall.view(ntok, -1), kp, vp, slots_all, f, nkv, hd, bs,
+                        k_scale=k_scale, v_scale=v_scale)
+        pools[f] = (kp, vp)
+        outs[f] = torch.empty((nseq * C, nq, hd), dtype=torch.bfloat16, device=dev)
+    del kall, vall
+    stream = torch.cuda.current_stream()
+    ev = {f: [] for f in fmts}
+
+    def step(record=False):
+        for f in fmts:
+            kp, vp = pools[f]
+            ops.cache_write(kc.view(nseq * C, -1), vc.view(nseq * C, -1), kp, vp, sc, f, nkv, hd, bs,
+                            k_scale=k_scale, v_scale=v_scale)
+            if record:
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+            ops.paged_prefill(q, cu, C, kp, vp, tables, lens, f, nkv, bs, out=outs[f],
+                              k_scale=k_scale, v_scale=v_scale)
+            if record:
+                a1.record(stream)
+                ev[f].append((a0, a1))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    ms_step, = slowest_rank([t0.elapsed_time(t1) / args.steps], dev)
+    flops = prefill_flops(lens_np, C, nq, hd)
+    per_layer = {}
+    for f in fmts:
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev[f]) * 1e3
+        cache_b = algorithmic_decode_bytes(f, lens_np, nkv, hd, bs)
+        per_layer[f] = {"us_per_layer": round(us, 2), "tflops": round(flops / (us * 1e-6) / 1e12, 2),
+                        "cache_bytes": cache_b}
+    dom = max(per_layer, key=lambda k: per_layer[k]["us_per_layer"])
+    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = pk.get("bf16_tflops") or 1900.0
+    tf_step = job_rate(flops * len(fmts), ws, ms_step) / 1e3
+    if rank == 0:
+        print(json.dumps({
+            "metric": "chunked-prefill attention TFLOP/s (algorithmic), us/layer", "value": round(tf_step, 2),
+            "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16/bf16 hi+lo operands, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC["prefill"].format(nseq=nseq), "formats": fmts,
+                       "l2": "caches far above L2 between steps",
+                       "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
+            "per_layer": per_layer,
+            "roofline": {"kernel": f"prefill_tc_kernel ({dom})", "bound": "tensor",
+                         "achieved": per_layer[dom]["tflops"], "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(per_layer[dom]["tflops"] / peak, 4), "traffic": None,
+                         "peak_kind": "measured bf16 dense, burst" if pk else "fallback",
+                         "flops_per_layer": flops},
+            "gpu_launches": 2 * len(fmts) * args.steps, "clocks": clocks}))
+
+
 def run_reference(args):
     ws, rank, _ = dist_info()
     if rank != 0:
@@ -481,6 +608,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_gpu(args)
 

@@ -26,6 +26,11 @@ Workloads (sizes follow the quantized-KV-cache pages' use cases):
   a seeded random permutation of the pool; then decode over 16 sequences x
   8192 with 32 query heads; K, V, Q N(0,1) bf16; formats turbo2 and turbo8.
 
+* ``prefill``: chunked prefill, Llama-3-8B-shaped: 8 sequences x 4096
+  positions whose last 512 are the new chunk (written, then attended
+  causally), 32 query / 8 KV heads, head_dim 128, llama8b's value
+  distribution; formats bf16, fp8, turbo4.
+
 Block tables are seeded permutations of the physical block ids, sliced per
 sequence, so no two sequences share a block.
 """
@@ -54,6 +59,7 @@ class Workload:
     extra_blocks: int = 0         # spare physical blocks beyond what the seqs need
     write_tokens: int = 0         # tokens written by the write step (gemma_write)
     write_row_elems: int = 0      # elements in one fused QKV row (key/value stride)
+    chunk: int = 0                # chunked prefill: new query tokens per sequence
     seed: int = 0
     notes: dict = field(default_factory=dict)
 
@@ -91,6 +97,9 @@ def make(name, seed=0, **over):
         w = Workload("gemma_write", 16, np.full(16, 8192, np.int32), 32, 16, 256, 16,
                      ("turbo2", "turbo8"), "bf16", outlier_frac=0.0,
                      write_tokens=8192, write_row_elems=(32 + 16 + 16) * 256)
+    elif name == "prefill":
+        w = Workload("prefill", 8, np.full(8, 4096, np.int32), 32, 8, 128, 16,
+                     ("bf16", "fp8", "turbo4"), "bf16", lognormal_sigma=0.5, chunk=512)
     else:
         raise KeyError(name)
     w.seed = seed
