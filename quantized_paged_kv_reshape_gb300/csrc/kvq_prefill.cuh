@@ -47,16 +47,18 @@ struct PfCfg {
   static constexpr int NT = 32 * NW;
   static constexpr int ROWS = 64;
   static constexpr int PITCH = HD + 8;                       // halves per plane row
+  static constexpr int NSUB = 1;  // 16-token sub-slabs per stage (2 measured slower on GB300)
+  static constexpr int TOK = 16 * NSUB;                      // tokens per stage
   static constexpr int KROW = SideGeom<KS, HD>::ROW, KSROW = SideGeom<KS, HD>::SROW;
   static constexpr int VROW = SideGeom<VS, HD>::ROW, VSROW = SideGeom<VS, HD>::SROW;
-  // raw stage: [16][KROW] [16][KSROW] [16][VROW] [16][VSROW], 16-byte aligned parts
-  static constexpr int R_KS = align_up(16 * KROW, 16);
-  static constexpr int R_V = R_KS + align_up(16 * KSROW, 16);
-  static constexpr int R_VS = R_V + align_up(16 * VROW, 16);
-  static constexpr int RAW = R_VS + align_up(16 * VSROW, 16);
+  // raw stage: [TOK][KROW] [TOK][KSROW] [TOK][VROW] [TOK][VSROW], 16-byte aligned parts
+  static constexpr int R_KS = align_up(TOK * KROW, 16);
+  static constexpr int R_V = R_KS + align_up(TOK * KSROW, 16);
+  static constexpr int R_VS = R_V + align_up(TOK * VROW, 16);
+  static constexpr int RAW = R_VS + align_up(TOK * VSROW, 16);
   // shared memory map (bytes)
   static constexpr int QPLANE = ROWS * PITCH * 2;
-  static constexpr int KPLANE = 16 * PITCH * 2;
+  static constexpr int KPLANE = TOK * PITCH * 2;
   static constexpr int OFF_Q = 0;                                   // q hi, q lo
   static constexpr int OFF_K = OFF_Q + 2 * QPLANE;                  // k planes
   static constexpr int OFF_V = OFF_K + PfSide<KS>::PLANES * KPLANE; // v planes
@@ -146,11 +148,11 @@ prefill_tc_kernel(const PrefillArgs a, const Codebooks cb) {
   uint16_t* qh_s = reinterpret_cast<uint16_t*>(smem + C::OFF_Q);
   uint16_t* ql_s = qh_s + C::ROWS * PITCH;
   uint16_t* kh_s = reinterpret_cast<uint16_t*>(smem + C::OFF_K);
-  uint16_t* kl_s = kh_s + 16 * PITCH;          // used when KP::PLANES == 2
+  uint16_t* kl_s = kh_s + C::TOK * PITCH;     // used when KP::PLANES == 2
   uint16_t* vh_s = reinterpret_cast<uint16_t*>(smem + C::OFF_V);
-  uint16_t* vl_s = vh_s + 16 * PITCH;          // used when VP::PLANES == 2
+  uint16_t* vl_s = vh_s + C::TOK * PITCH;     // used when VP::PLANES == 2
   uint8_t* raw = smem + C::OFF_RAW;
-  uint8_t* vrow_s = smem + C::OFF_OFFS;        // [2][16] row valid flags
+  uint8_t* vrow_s = smem + C::OFF_OFFS;        // [2][TOK] row valid flags
   float* lv = reinterpret_cast<float*>(smem + C::OFF_LV);   // [K, V][hi, lo][16]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -206,10 +208,10 @@ prefill_tc_kernel(const PrefillArgs a, const Codebooks cb) {
   float m[2] = {-CUDART_INF_F, -CUDART_INF_F}, l[2] = {0.f, 0.f};
   const int p_first = max(pbase, 0);
   const int lo_first = a.window > 0 ? max(0, p_first + 1 - a.window) : 0;
-  const int slab_begin = lo_first >> 4;
-  const int slab_end = p_last >= 0 ? (p_last >> 4) + 1 : slab_begin;
+  const int slab_begin = lo_first / C::TOK;
+  const int slab_end = p_last >= 0 ? p_last / C::TOK + 1 : slab_begin;
 
-  // Copy the K/V rows of slab `sl` (positions 16 sl .. 16 sl + 15) into raw
+  // Copy the K/V rows of slab `sl` (positions TOK sl .. TOK sl + TOK - 1) into raw
   // buffer b; rows outside [0, len) or with a bad block id are zero-filled
   // and flagged invalid.
   auto row_src = [&](int pos, int64_t& blk, int64_t& rr) -> bool {
@@ -223,11 +225,11 @@ prefill_tc_kernel(const PrefillArgs a, const Codebooks cb) {
                        auto rowbytes_c, auto chunk_c) {
     constexpr int RB = decltype(rowbytes_c)::value, CHB = decltype(chunk_c)::value;
     if constexpr (RB > 0) {
-      constexpr int NC = RB / CHB, TOT = 16 * NC;
+      constexpr int NC = RB / CHB, TOT = C::TOK * NC;
       for (int q = tid; q < TOT; q += NT) {
         const int row = q / NC, ch = q - row * NC;
         int64_t blk = 0, rr = 0;
-        const bool ok = row_src(sl * 16 + row, blk, rr);
+        const bool ok = row_src(sl * C::TOK + row, blk, rr);
         const int64_t src = ok ? blk * stride + sec + rr * RB : 0;
         cp_async<CHB>(dst + row * RB + ch * CHB, cache + src + ch * CHB, ok);
       }
@@ -247,9 +249,9 @@ prefill_tc_kernel(const PrefillArgs a, const Codebooks cb) {
     copy_part(rb + C::R_VS, a.v_cache, a.v_bstride, a.v_dsec, sl,
               std::integral_constant<int, VG::SROW>{},
               std::integral_constant<int, (VG::SCH > 0 ? VG::SCH : 1)>{});
-    if (tid < 16) {
+    if (tid < C::TOK) {
       int64_t blk, rr;
-      vrow_s[b * 16 + tid] = row_src(sl * 16 + tid, blk, rr) ? 1 : 0;
+      vrow_s[b * C::TOK + tid] = row_src(sl * C::TOK + tid, blk, rr) ? 1 : 0;
     }
   };
 
@@ -265,10 +267,11 @@ prefill_tc_kernel(const PrefillArgs a, const Codebooks cb) {
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();  // slab sl staged by every thread; the planes are free
-    {  // dequantize both sides of the 16 rows into the operand planes
+#pragma unroll
+    for (int u = 0; u < C::NSUB; ++u) {  // dequantize both sides into the operand planes
       const uint8_t* rb = raw + b * C::RAW;
       constexpr int TPR = HD / EPT;  // threads per row
-      const int row = tid / TPR, d0 = (tid - row * TPR) * EPT;
+      const int row = u * 16 + tid / TPR, d0 = (tid % TPR) * EPT;
       uint32_t hw[EPT / 2], lw[EPT / 2];
       pf_dequant<KS, HD, EPT>(rb + row * C::KROW, rb + C::R_KS + row * C::KSROW, d0, lv, lv + 16,
                               hw, lw);
@@ -287,101 +290,104 @@ prefill_tc_kernel(const PrefillArgs a, const Codebooks cb) {
     }
     __syncthreads();
 
-    // ---- S = Q . K^T for this warp's 16 rows and the slab's 16 positions
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
-      const uint16_t* qa = qh_s + (rw + (lane & 15)) * PITCH + (lane >> 4) * 8;
-      const uint16_t* qb = ql_s + (rw + (lane & 15)) * PITCH + (lane >> 4) * 8;
-      const int krow = (lane & 7) + ((lane >> 4) << 3), kofs = ((lane >> 3) & 1) * 8;
-#pragma unroll
-      for (int j = 0; j < HD / 16; ++j) {
-        uint32_t ah[4], al[4], bk[4];
-        tc::ldsm_x4(ah, qa + j * 16);
-        tc::ldsm_x4(al, qb + j * 16);
-        tc::ldsm_x4(bk, kh_s + krow * PITCH + j * 16 + kofs);
-        tc::mma<KP::BF>(sc[0], ah[0], ah[1], ah[2], ah[3], bk[0], bk[1]);
-        tc::mma<KP::BF>(sc[1], ah[0], ah[1], ah[2], ah[3], bk[2], bk[3]);
-        tc::mma<KP::BF>(sc[0], al[0], al[1], al[2], al[3], bk[0], bk[1]);
-        tc::mma<KP::BF>(sc[1], al[0], al[1], al[2], al[3], bk[2], bk[3]);
-        if constexpr (KP::PLANES == 2) {
-          uint32_t bl[4];
-          tc::ldsm_x4(bl, kl_s + krow * PITCH + j * 16 + kofs);
-          tc::mma<KP::BF>(sc[0], ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
-          tc::mma<KP::BF>(sc[1], ah[0], ah[1], ah[2], ah[3], bl[2], bl[3]);
+#pragma unroll 1
+    for (int u = 0; u < C::NSUB; ++u) {  // 16-token sub-slabs
+      // ---- S = Q . K^T for this warp's 16 rows and the slab's 16 positions
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const uint16_t* qa = qh_s + (rw + (lane & 15)) * PITCH + (lane >> 4) * 8;
+        const uint16_t* qb = ql_s + (rw + (lane & 15)) * PITCH + (lane >> 4) * 8;
+        const int krow = (lane & 7) + ((lane >> 4) << 3), kofs = ((lane >> 3) & 1) * 8;
+  #pragma unroll
+        for (int j = 0; j < HD / 16; ++j) {
+          uint32_t ah[4], al[4], bk[4];
+          tc::ldsm_x4(ah, qa + j * 16);
+          tc::ldsm_x4(al, qb + j * 16);
+          tc::ldsm_x4(bk, kh_s + (u * 16 + krow) * PITCH + j * 16 + kofs);
+          tc::mma<KP::BF>(sc[0], ah[0], ah[1], ah[2], ah[3], bk[0], bk[1]);
+          tc::mma<KP::BF>(sc[1], ah[0], ah[1], ah[2], ah[3], bk[2], bk[3]);
+          tc::mma<KP::BF>(sc[0], al[0], al[1], al[2], al[3], bk[0], bk[1]);
+          tc::mma<KP::BF>(sc[1], al[0], al[1], al[2], al[3], bk[2], bk[3]);
+          if constexpr (KP::PLANES == 2) {
+            uint32_t bl[4];
+            tc::ldsm_x4(bl, kl_s + (u * 16 + krow) * PITCH + j * 16 + kofs);
+            tc::mma<KP::BF>(sc[0], ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+            tc::mma<KP::BF>(sc[1], ah[0], ah[1], ah[2], ah[3], bl[2], bl[3]);
+          }
         }
       }
-    }
-    // ---- mask (causal, window, invalid rows) and online softmax
-    const uint8_t* vr = vrow_s + b * 16;
-    float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {          // rows g, g + 8
-      const int r = rw + g + 8 * h;
-      const int qi = r / rp;
-      const int p = pbase + qi;
-      const bool row_ok = qi < nq_tile && (r - qi * rp) < a.rep;
-      const int lo_p = a.window > 0 ? p + 1 - a.window : 0;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int tk = nt * 8 + 2 * c + e;
-          const int t = sl * 16 + tk;
-          const bool ok = row_ok && t <= p && t >= lo_p && vr[tk];
-          float& v = sc[nt][2 * h + e];
-          v = ok ? v * scale : -CUDART_INF_F;
-          mx[h] = fmaxf(mx[h], v);
+      // ---- mask (causal, window, invalid rows) and online softmax
+      const uint8_t* vr = vrow_s + b * C::TOK + u * 16;
+      float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+  #pragma unroll
+      for (int h = 0; h < 2; ++h) {          // rows g, g + 8
+        const int r = rw + g + 8 * h;
+        const int qi = r / rp;
+        const int p = pbase + qi;
+        const bool row_ok = qi < nq_tile && (r - qi * rp) < a.rep;
+        const int lo_p = a.window > 0 ? p + 1 - a.window : 0;
+  #pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+  #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tk = nt * 8 + 2 * c + e;
+            const int t = sl * C::TOK + u * 16 + tk;
+            const bool ok = row_ok && t <= p && t >= lo_p && vr[tk];
+            float& v = sc[nt][2 * h + e];
+            v = ok ? v * scale : -CUDART_INF_F;
+            mx[h] = fmaxf(mx[h], v);
+          }
         }
       }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-    }
-    float pr[2][4];
-    float al_[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float mn = fmaxf(m[h], mx[h]);
-      al_[h] = mn == -CUDART_INF_F ? 1.f : exp2f(m[h] - mn);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float v = sc[nt][2 * h + e];
-          pr[nt][2 * h + e] = (mn == -CUDART_INF_F || v == -CUDART_INF_F) ? 0.f : exp2f(v - mn);
-        }
-      l[h] = l[h] * al_[h] + (pr[0][2 * h] + pr[0][2 * h + 1]) + (pr[1][2 * h] + pr[1][2 * h + 1]);
-      m[h] = mn;
-    }
-#pragma unroll
-    for (int i = 0; i < NDT; ++i) {
-      o[i][0] *= al_[0]; o[i][1] *= al_[0]; o[i][2] *= al_[1]; o[i][3] *= al_[1];
-    }
-    // ---- O += P . V (P from the S accumulators: the m16n8 C layout of two
-    // n-tiles is the m16k16 A layout)
-    uint32_t ph[4], pl[4];
-    tc::split2<VP::BF>(pr[0][0], pr[0][1], ph[0], pl[0]);
-    tc::split2<VP::BF>(pr[0][2], pr[0][3], ph[1], pl[1]);
-    tc::split2<VP::BF>(pr[1][0], pr[1][1], ph[2], pl[2]);
-    tc::split2<VP::BF>(pr[1][2], pr[1][3], ph[3], pl[3]);
-    {
-      const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vofs = (lane >> 4) * 8;
-#pragma unroll
-      for (int i = 0; i < NDT; i += 2) {
-        const int d = dh * (HD / DS) + i * 8;
-        uint32_t bv[4];
-        tc::ldsm_x4_t(bv, vh_s + vrow * PITCH + d + vofs);
-        tc::mma<VP::BF>(o[i], ph[0], ph[1], ph[2], ph[3], bv[0], bv[1]);
-        tc::mma<VP::BF>(o[i + 1], ph[0], ph[1], ph[2], ph[3], bv[2], bv[3]);
-        tc::mma<VP::BF>(o[i], pl[0], pl[1], pl[2], pl[3], bv[0], bv[1]);
-        tc::mma<VP::BF>(o[i + 1], pl[0], pl[1], pl[2], pl[3], bv[2], bv[3]);
-        if constexpr (VP::PLANES == 2) {
-          uint32_t bw[4];
-          tc::ldsm_x4_t(bw, vl_s + vrow * PITCH + d + vofs);
-          tc::mma<VP::BF>(o[i], ph[0], ph[1], ph[2], ph[3], bw[0], bw[1]);
-          tc::mma<VP::BF>(o[i + 1], ph[0], ph[1], ph[2], ph[3], bw[2], bw[3]);
+  #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+      }
+      float pr[2][4];
+      float al_[2];
+  #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float mn = fmaxf(m[h], mx[h]);
+        al_[h] = mn == -CUDART_INF_F ? 1.f : exp2f(m[h] - mn);
+  #pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float v = sc[nt][2 * h + e];
+            pr[nt][2 * h + e] = (mn == -CUDART_INF_F || v == -CUDART_INF_F) ? 0.f : exp2f(v - mn);
+          }
+        l[h] = l[h] * al_[h] + (pr[0][2 * h] + pr[0][2 * h + 1]) + (pr[1][2 * h] + pr[1][2 * h + 1]);
+        m[h] = mn;
+      }
+  #pragma unroll
+      for (int i = 0; i < NDT; ++i) {
+        o[i][0] *= al_[0]; o[i][1] *= al_[0]; o[i][2] *= al_[1]; o[i][3] *= al_[1];
+      }
+      // ---- O += P . V (P from the S accumulators: the m16n8 C layout of two
+      // n-tiles is the m16k16 A layout)
+      uint32_t ph[4], pl[4];
+      tc::split2<VP::BF>(pr[0][0], pr[0][1], ph[0], pl[0]);
+      tc::split2<VP::BF>(pr[0][2], pr[0][3], ph[1], pl[1]);
+      tc::split2<VP::BF>(pr[1][0], pr[1][1], ph[2], pl[2]);
+      tc::split2<VP::BF>(pr[1][2], pr[1][3], ph[3], pl[3]);
+      {
+        const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vofs = (lane >> 4) * 8;
+  #pragma unroll
+        for (int i = 0; i < NDT; i += 2) {
+          const int d = dh * (HD / DS) + i * 8;
+          uint32_t bv[4];
+          tc::ldsm_x4_t(bv, vh_s + (u * 16 + vrow) * PITCH + d + vofs);
+          tc::mma<VP::BF>(o[i], ph[0], ph[1], ph[2], ph[3], bv[0], bv[1]);
+          tc::mma<VP::BF>(o[i + 1], ph[0], ph[1], ph[2], ph[3], bv[2], bv[3]);
+          tc::mma<VP::BF>(o[i], pl[0], pl[1], pl[2], pl[3], bv[0], bv[1]);
+          tc::mma<VP::BF>(o[i + 1], pl[0], pl[1], pl[2], pl[3], bv[2], bv[3]);
+          if constexpr (VP::PLANES == 2) {
+            uint32_t bw[4];
+            tc::ldsm_x4_t(bw, vl_s + (u * 16 + vrow) * PITCH + d + vofs);
+            tc::mma<VP::BF>(o[i], ph[0], ph[1], ph[2], ph[3], bw[0], bw[1]);
+            tc::mma<VP::BF>(o[i + 1], ph[0], ph[1], ph[2], ph[3], bw[2], bw[3]);
+          }
         }
       }
     }
