@@ -125,6 +125,46 @@ def test_decode_rejects_bad_arguments():
     assert _decode(sliding_window=-5) == A.KVQ_ERR_ARG
 
 
+def _prefill(**over):
+    args = dict(q=16, q_dtype=A.KVQ_DTYPE_BF16, q_stride=4096, cu_q=32, max_chunk=64,
+                k_cache=4096, v_cache=4096, out=64, out_dtype=A.KVQ_DTYPE_F32, block_tables=128,
+                max_blocks_per_seq=4, seq_lens=256, num_seqs=2, num_blocks=8, num_q_heads=32,
+                num_kv_heads=8, head_dim=128, block_size=16, k_block_stride_bytes=65536,
+                v_block_stride_bytes=65536, sm_scale=0.0, k_scale=1.0, v_scale=1.0,
+                sliding_window=0, fmt=0, error_flag=None, stream=None)
+    args.update(over)
+    with pytest.raises(A.KvqError) as e:
+        A.kvq_paged_prefill(**args)
+    return e.value.status
+
+
+def test_prefill_rejects_bad_arguments():
+    """Host-side validation, before any launch (these calls never reach CUDA)."""
+    assert _prefill(num_q_heads=30) == A.KVQ_ERR_SHAPE
+    assert _prefill(num_q_heads=128) == A.KVQ_ERR_SHAPE
+    assert _prefill(block_size=64) == A.KVQ_ERR_SHAPE
+    assert _prefill(head_dim=80) == A.KVQ_ERR_SHAPE
+    assert _prefill(cu_q=None) == A.KVQ_ERR_ARG
+    assert _prefill(max_chunk=-1) == A.KVQ_ERR_ARG
+    assert _prefill(q_stride=100) == A.KVQ_ERR_ARG
+    assert _prefill(k_cache=4104) == A.KVQ_ERR_ALIGN
+    assert _prefill(k_block_stride_bytes=1024) == A.KVQ_ERR_ARG
+    assert _prefill(fmt=1, k_scale=0.0) == A.KVQ_ERR_ARG
+    assert _prefill(fmt=42) == A.KVQ_ERR_FORMAT
+    assert _prefill(q_dtype=9) == A.KVQ_ERR_FORMAT
+
+
+def test_prefill_nothing_to_do_is_ok():
+    """No sequences or an empty chunk bound: success without a launch."""
+    A.kvq_paged_prefill(q=16, q_dtype=A.KVQ_DTYPE_F32, q_stride=4096, cu_q=32, max_chunk=0,
+                        k_cache=4096, v_cache=4096, out=64, out_dtype=A.KVQ_DTYPE_F32,
+                        block_tables=128, max_blocks_per_seq=4, seq_lens=256, num_seqs=2,
+                        num_blocks=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, k_block_stride_bytes=65536, v_block_stride_bytes=65536,
+                        sm_scale=0.0, k_scale=1.0, v_scale=1.0, sliding_window=0, fmt=0,
+                        error_flag=None, stream=None)
+
+
 def test_workspace_formula():
     """Partials [num_seqs][nq][kmax][hd + 4] fp32, then int32 partial counts
     [num_seqs][nkv] (16-byte padded); kmax >= 2 (a unit cut once) and never
