@@ -167,26 +167,28 @@ int sm_count() {
   return n;
 }
 
-// Decode partition.  The decode runs persistent CTAs, two per SM: R per kv
-// head, each on an equal share of the sequences' 16-token slabs, at least
+// Decode partition.  The decode runs persistent CTAs, two or three per SM
+// depending on the instance: R per kv head, each on an equal share of the sequences' 16-token slabs, at least
 // min_slabs of them (measured on GB300: one balanced wave of long CTAs beats
 // more, shorter split CTAs, which pay the prologue and merge more often and
 // leave a partial last wave).  kmax bounds the partials of one (sequence,
 // kv head) row: a row of n slabs spans at most floor((n - 1) / per_cta) + 2
 // CTAs, with per_cta >= max(min_slabs, n / R).
 struct DecodePlan {
-  int ranges, min_slabs, kmax;
+  int sms, max_ranges, min_slabs, kmax;
 };
 
+// At most 4 CTAs per SM for any instance (the launcher picks its own count).
 DecodePlan plan_decode(int nkv, int bs, int max_blocks, int window, int sms) {
   DecodePlan p{};
-  p.ranges = std::max(1, 2 * (sms > 0 ? sms : 148) / std::max(1, nkv));
+  p.sms = sms > 0 ? sms : 148;
+  p.max_ranges = std::max(1, 4 * p.sms / std::max(1, nkv));
   p.min_slabs = 16;
   int64_t max_n = ((int64_t)max_blocks * bs + 15) / 16;
   if (window > 0) max_n = std::min<int64_t>(max_n, (window + 15) / 16 + 1);
   if (max_n < 1) max_n = 1;
   const int64_t by_len = (max_n - 1) / p.min_slabs + 2;
-  p.kmax = (int)std::min<int64_t>(by_len, p.ranges + 1);
+  p.kmax = (int)std::min<int64_t>(by_len, p.max_ranges + 1);
   return p;
 }
 
@@ -419,7 +421,8 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   a.inv_sqrt_hd = (float)(1.0 / std::sqrt((double)hd));
   a.window = window;
   a.sparse_thr = sparse_v_threshold;
-  a.ranges = p.ranges;
+  a.sms = p.sms;
+  a.max_ranges = p.max_ranges;
   a.min_slabs = p.min_slabs;
   a.kmax = p.kmax;
   a.part = (float*)workspace;

@@ -171,10 +171,19 @@ struct TcSide {
 #ifndef KVQ_TC_NW_RAW
 #define KVQ_TC_NW_RAW 8
 #endif
+#ifndef KVQ_TC_NW_BF16
+#define KVQ_TC_NW_BF16 4
+#endif
+#ifndef KVQ_TC_NST_MAX
+#define KVQ_TC_NST_MAX 6
+#endif
+#ifndef KVQ_TC_CPS_BF16
+#define KVQ_TC_CPS_BF16 2
+#endif
 template <int KS, int VS, int HD>
 struct TcWarps {
   static constexpr bool CBS = side_codebook(KS) || side_codebook(VS);
-  static constexpr int NW = HD > 128 ? 4 : CBS ? KVQ_TC_NW_CB : (KS == S_BF16 ? 4 : KVQ_TC_NW_RAW);
+  static constexpr int NW = HD > 128 ? 4 : CBS ? KVQ_TC_NW_CB : (KS == S_BF16 ? KVQ_TC_NW_BF16 : KVQ_TC_NW_RAW);
 };
 
 template <int KS, int VS, int HD>
@@ -202,9 +211,12 @@ struct TcCfg {
   static constexpr int OFF_STATE = OFF_SCAN + 16 * 8;          // partition scan / merge scratch
   static constexpr int OFF_LUT = OFF_STATE + 8 * 8;            // CTA loop state
   static constexpr int OFF_RING = OFF_LUT + LUTS;
-  static constexpr int BUDGET = 112 * 1024 - OFF_RING;         // two CTAs per SM
+  // CTAs per SM: BF16 K (light per-slab work, latency bound per warp) runs
+  // KVQ_TC_CPS_BF16 CTAs with shallower rings, the others two.
+  static constexpr int CPS = (KS == S_BF16 && HD <= 128) ? KVQ_TC_CPS_BF16 : 2;
+  static constexpr int BUDGET = (228 - CPS) * 1024 / CPS - OFF_RING;
   static constexpr int NST0 = BUDGET / (NW * STAGE);
-  static constexpr int NST = NST0 > 6 ? 6 : (NST0 < 2 ? 2 : NST0);
+  static constexpr int NST = NST0 > KVQ_TC_NST_MAX ? KVQ_TC_NST_MAX : (NST0 < 2 ? 2 : NST0);
   static constexpr int RING = NW * NST * STAGE;
   static constexpr int MERGE = NW * 8 * HD * 4 + NW * 8 * 2 * 4;
   static constexpr int SMEM = OFF_RING + (RING > MERGE ? RING : MERGE);
@@ -1083,9 +1095,10 @@ cudaError_t launch_tc_kern(const DecodeArgs& a, const Codebooks& cb, cudaStream_
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
   }
-  // a.ranges CTAs per kv head fill two CTAs per SM; instances whose stages
-  // need more than half of an SM's shared memory run one per SM.
-  const int ranges = C::SMEM <= 113 * 1024 ? a.ranges : (a.ranges + 1) / 2;
+  // C::CPS CTAs per SM (one when the stages need more than half of an SM's
+  // shared memory); never more CTAs per kv head than the host planned for.
+  const int cps = C::SMEM <= (228 - C::CPS) * 1024 / C::CPS ? C::CPS : 1;
+  const int ranges = max(1, min(a.max_ranges, cps * a.sms / a.nkv));
   const int grid = ranges * a.nkv;
   kern<<<grid, 32 * C::NW, C::SMEM, st>>>(a, cb);
   return cudaGetLastError();

@@ -49,7 +49,8 @@ struct DecodeArgs {  // arguments of the paged decode (decode_tc_kernel)
   float inv_sqrt_hd;
   int32_t window;
   float sparse_thr;
-  int32_t ranges;         // CTAs per kv head at two CTAs per SM (halved when one fits)
+  int32_t sms;            // SMs of the device
+  int32_t max_ranges;     // upper bound of the CTAs per kv head (sizes kmax)
   int32_t min_slabs;      // lower bound of the slabs per CTA
   int32_t kmax;           // partial slots per (sequence, query head)
   float* part;            // [num_seqs][nq][kmax][head_dim + 4] fp32: m, l, -, -, acc[head_dim]
