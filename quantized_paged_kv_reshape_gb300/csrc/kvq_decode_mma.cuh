@@ -478,10 +478,52 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       }
     }
   };
+  // Fast path of a slab whose 16 positions are all attended and lie in one
+  // page (block_size >= 16) or two (block_size 8), both valid: the rows of
+  // one (side, kv head) are nkv * row-bytes apart inside a page, so each lane
+  // forms its chunks' source addresses directly from the page base.
+  auto copy_fast = [&](uint8_t* dst, int dst_stride, const uint8_t* cache, int64_t bstride,
+                       int64_t sec, int slab_pos, int ba, int bb, auto rowbytes_c, auto chunk_c) {
+    constexpr int RB = decltype(rowbytes_c)::value, CHB = decltype(chunk_c)::value;
+    constexpr int NC = RB / CHB, RPI = 32 / NC, PASSES = (SLAB + RPI - 1) / RPI;
+    const int r0 = lane / NC, ch = lane - r0 * NC;
+    const int64_t rowstep = (int64_t)nkv * RB;
+#pragma unroll
+    for (int k = 0; k < PASSES; ++k) {
+      const int row = r0 + RPI * k;
+      if (RPI * PASSES == SLAB || row < SLAB) {
+        const int64_t blk = row < 8 ? ba : bb;
+        const int64_t src = blk * bstride + sec + (int64_t)((slab_pos + row) & (bs - 1)) * rowstep +
+                            (int64_t)kvh * RB + ch * CHB;
+        cp_async<CHB>(dst + row * dst_stride + ch * CHB, cache + src, true);
+      }
+    }
+  };
   auto issue = [&](int s) {
     __syncwarp();  // the previous issue's reads of offs are done
     uint8_t* sb = ring + (s % C::NST) * C::STAGE;
     const int slab_pos = tok0 + (warp + NW * s) * SLAB;
+    constexpr bool FAST = (32 % (KT::ROW / KT::CH) == 0) && (32 % (VT::ROW / VT::CH) == 0) &&
+                          (KT::SROW == 0 || 32 % (KT::SROW / KT::SCH) == 0) &&
+                          (VT::SROW == 0 || 32 % (VT::SROW / VT::SCH) == 0);
+    if constexpr (FAST) {
+      if (slab_pos >= lo && slab_pos + SLAB <= tok_end) {
+        const int ba = blk_s[(slab_pos >> lbs) - p0], bb = blk_s[((slab_pos + 8) >> lbs) - p0];
+        if (ba >= 0 && bb >= 0) {   // warp-uniform
+          copy_fast(sb, KT::KRS, a.k_cache, a.k_bstride, 0, slab_pos, ba, bb,
+                    std::integral_constant<int, KT::ROW>{}, std::integral_constant<int, KT::CH>{});
+          if constexpr (KT::SROW > 0)
+            copy_fast(sb + C::OFF_KS, KT::SROW, a.k_cache, a.k_bstride, a.k_dsec, slab_pos, ba, bb,
+                      std::integral_constant<int, KT::SROW>{}, std::integral_constant<int, KT::SCH>{});
+          copy_fast(sb + C::OFF_V, VT::VRS, a.v_cache, a.v_bstride, 0, slab_pos, ba, bb,
+                    std::integral_constant<int, VT::ROW>{}, std::integral_constant<int, VT::CH>{});
+          if constexpr (VT::SROW > 0)
+            copy_fast(sb + C::OFF_VS, VT::SROW, a.v_cache, a.v_bstride, a.v_dsec, slab_pos, ba, bb,
+                      std::integral_constant<int, VT::SROW>{}, std::integral_constant<int, VT::SCH>{});
+          return;
+        }
+      }
+    }
     const int b = pos_block(slab_pos + lane);
     const int64_t rr = (int64_t)((slab_pos + lane) & (bs - 1)) * nkv + kvh;   // row in block
     const int64_t bk = (int64_t)b * a.k_bstride, bv = (int64_t)b * a.v_bstride;
