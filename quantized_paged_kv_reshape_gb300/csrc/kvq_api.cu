@@ -167,13 +167,16 @@ int sm_count() {
   return n;
 }
 
-// Decode partition.  The decode runs persistent CTAs, two or three per SM
-// depending on the instance: R per kv head, each on an equal share of the sequences' 16-token slabs, at least
-// min_slabs of them (measured on GB300: one balanced wave of long CTAs beats
-// more, shorter split CTAs, which pay the prologue and merge more often and
-// leave a partial last wave).  kmax bounds the partials of one (sequence,
-// kv head) row: a row of n slabs spans at most floor((n - 1) / per_cta) + 2
-// CTAs, with per_cta >= max(min_slabs, n / R).
+// Decode partition.  The decode runs persistent CTAs, two per SM (the
+// launcher picks the instance's count, at most four): R per kv head, each
+// on an equal share of the sequences' 16-token slabs (measured on GB300: one
+// balanced wave of long CTAs beats more, shorter split CTAs, which pay the
+// prologue and merge more often and leave a partial last wave).  kmax is the
+// number of partial slots per (sequence, query head): a row of n slabs spans
+// at most floor((n - 1) / per_cta) + 2 CTAs, and the kernel keeps per_cta >=
+// max_n / (kmax - 1) for the longest row max_n.  Here kmax = min(R_max + 1,
+// (max_n_bound - 1) / 16 + 2): with at least 16 slabs per CTA for the longest
+// possible row, or one slot per CTA of a head.
 struct DecodePlan {
   int sms, max_ranges, min_slabs, kmax;
 };
@@ -423,7 +426,6 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   a.sparse_thr = sparse_v_threshold;
   a.sms = p.sms;
   a.max_ranges = p.max_ranges;
-  a.min_slabs = p.min_slabs;
   a.kmax = p.kmax;
   a.part = (float*)workspace;
   a.counters = (int32_t*)((uint8_t*)workspace + part_bytes(num_seqs, nq, hd, p));

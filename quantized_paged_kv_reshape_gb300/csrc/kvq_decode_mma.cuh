@@ -358,7 +358,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   // ---- Partition.  Each kv head gets R = gridDim.x / nkv CTAs (the host
   // launches a multiple of nkv).  The sequences' 16-token slabs are laid end
   // to end (S in all); CTA (h, j) takes slabs [j * cpc, (j + 1) * cpc) of
-  // kv head h, cpc = max(ceil(S / R), min_slabs), so every CTA gets the same
+  // kv head h, cpc about ceil(S / R) (see below), so every CTA gets the same
   // amount of work whatever the lengths, and the CTAs of the different kv
   // heads read the same token positions at the same time (their rows share
   // DRAM sectors, the scale rows especially).  A (sequence, kv head) row cut
@@ -370,10 +370,12 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   const int chunk = (N + NT - 1) / NT;
   const int s_beg = min(N, tid * chunk), s_end = min(N, s_beg + chunk);
   int64_t mine = 0;
+  int longest = 0;
   for (int s = s_beg; s < s_end; ++s) {
     int f, n, l_, e_;
     seq_slabs(s, f, n, l_, e_);
     mine += n;
+    longest = max(longest, n);
     if (blockIdx.x == 0 && a.seq_lens[s] > cap && a.err) atomicOr(a.err, 2);
   }
   int64_t incl = mine;
@@ -381,18 +383,25 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
   for (int d = 1; d < 32; d <<= 1) {
     const int64_t y = __shfl_up_sync(0xffffffffu, incl, d);
     if (lane >= d) incl += y;
+    longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, d));
   }
   if (lane == 31) scan_s[warp] = incl;
+  if (lane == 0) scan_s[8 + warp] = longest;
   __syncthreads();
-  int64_t before = 0, total = 0;
+  int64_t before = 0, total = 0, max_n = 0;
   for (int w2 = 0; w2 < NW; ++w2) {
     const int64_t v = scan_s[w2];
     if (w2 < warp) before += v;
     total += v;
+    max_n = max(max_n, scan_s[8 + w2]);
   }
   const int64_t excl = before + incl - mine;  // slabs before this thread's chunk
+  // Slabs per CTA: an equal share, but never so few that a row of max_n
+  // slabs spans more than kmax CTAs (the partial slots the host sized):
+  // a row of n slabs spans at most floor((n - 1) / cpc) + 2 CTAs.
   int64_t cpc = (total + R - 1) / R;
-  if (cpc < a.min_slabs) cpc = a.min_slabs;
+  if (a.kmax > 1) cpc = max(cpc, (max_n + a.kmax - 2) / (a.kmax - 1));
+  if (cpc < 1) cpc = 1;
   const int64_t x0 = (int64_t)jr * cpc;
   const int64_t x_end = min(x0 + cpc, total);
   __syncthreads();  // scan_s is reused below

@@ -51,7 +51,6 @@ struct DecodeArgs {  // arguments of the paged decode (decode_tc_kernel)
   float sparse_thr;
   int32_t sms;            // SMs of the device
   int32_t max_ranges;     // upper bound of the CTAs per kv head (sizes kmax)
-  int32_t min_slabs;      // lower bound of the slabs per CTA
   int32_t kmax;           // partial slots per (sequence, query head)
   float* part;            // [num_seqs][nq][kmax][head_dim + 4] fp32: m, l, -, -, acc[head_dim]
   int32_t* counters;      // [num_seqs][nkv] partials arrived; zero between calls
