@@ -57,9 +57,9 @@ WORKLOAD_DESC = {
 # decode launch, from the ncu capture summarised in profiles/ (None when the
 # kernel changed after the capture).
 TRAFFIC = {
-    ("llama8b", "bf16"): 542_208_768,
-    ("llama8b", "fp8"): 273_052_928,
-    ("llama8b", "turbo4"): 156_112_896,
+    ("llama8b", "bf16"): 541_731_328,
+    ("llama8b", "fp8"): 273_162_240,
+    ("llama8b", "turbo4"): 156_372_992,
 }
 
 
