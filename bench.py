@@ -559,7 +559,7 @@ def run_prefill(args):
                        "l2": "caches far above L2 between steps",
                        "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
             "per_layer": per_layer,
-            "roofline": {"kernel": f"prefill_tc_kernel ({dom})", "bound": "tensor",
+            "roofline": {"kernel": f"prefill_tc5_kernel ({dom})", "bound": "tensor",
                          "achieved": per_layer[dom]["tflops"], "peak": peak, "unit": "TFLOP/s",
                          "frac": round(per_layer[dom]["tflops"] / peak, 4), "traffic": None,
                          "peak_kind": "measured bf16 dense, burst" if pk else "fallback",

@@ -446,15 +446,4 @@ cudaError_t launch_prefill_inst(const PrefillArgs& a, const Codebooks& cb, int m
   return cudaGetLastError();
 }
 
-template <int KS, int VS>
-cudaError_t launch_prefill_pair(int hd, const PrefillArgs& a, const Codebooks& cb, int max_chunk,
-                                cudaStream_t st) {
-  switch (hd) {
-    case 64: return launch_prefill_inst<KS, VS, 64>(a, cb, max_chunk, st);
-    case 128: return launch_prefill_inst<KS, VS, 128>(a, cb, max_chunk, st);
-    case 256: return launch_prefill_inst<KS, VS, 256>(a, cb, max_chunk, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 }  // namespace kvq

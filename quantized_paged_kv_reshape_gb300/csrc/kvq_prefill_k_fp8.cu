@@ -2,7 +2,7 @@
 // per K side so the instances compile in parallel).  V sides: the
 // catalogue's pairs with this K side ("spark_runtime/kv_cache.rs",
 // KvCacheDtype::kv_pair).
-#include "kvq_prefill.cuh"
+#include "kvq_prefill_tc5.cuh"
 
 namespace kvq {
 
