@@ -100,6 +100,12 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&v)[16]) {
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
       "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
 }
+// 2^x (PTX ex2.approx.ftz: relative error ~2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
@@ -245,38 +251,36 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     rr = (int64_t)(pos & (a.bs - 1)) * a.nkv + kvh;
     return true;
   };
-  auto copy_part = [&](uint8_t* dst, const uint8_t* cache, int64_t stride, int64_t sec, int st,
-                       auto rowbytes_c, auto chunk_c) {
+  // Thread (row t = tid % TOK, part = tid / TOK) looks the row's block up
+  // once and copies chunks part, part + NT / TOK, ... of its four rows.
+  constexpr int PARTS = NT / TOK;
+  auto copy_row = [&](uint8_t* dst, const uint8_t* src, const uint8_t* base, bool ok, int part,
+                      auto rowbytes_c, auto chunk_c) {
     constexpr int RB = decltype(rowbytes_c)::value, CHB = decltype(chunk_c)::value;
     if constexpr (RB > 0) {
-      constexpr int NCH = RB / CHB, TOT = TOK * NCH;
-      for (int q = tid; q < TOT; q += NT) {
-        const int row = q / NCH, ch = q - row * NCH;
-        int64_t blk = 0, rr = 0;
-        const bool ok = row_src(st * TOK + row, blk, rr);
-        const int64_t src = ok ? blk * stride + sec + rr * RB : 0;
-        cp_async<CHB>(dst + row * RB + ch * CHB, cache + src + ch * CHB, ok);
-      }
+#pragma unroll
+      for (int ch = part; ch < RB / CHB; ch += PARTS)
+        cp_async<CHB>(dst + ch * CHB, (ok ? src : base) + ch * CHB, ok);
     }
   };
   auto issue = [&](int st, int b) {
     uint8_t* rb = raw + b * C::RAW;
     using KG = SideGeom<KS, HD>;
     using VG = SideGeom<VS, HD>;
-    copy_part(rb, a.k_cache, a.k_bstride, 0, st, std::integral_constant<int, KG::ROW>{},
-              std::integral_constant<int, KG::CH>{});
-    copy_part(rb + C::R_KS, a.k_cache, a.k_bstride, a.k_dsec, st,
-              std::integral_constant<int, KG::SROW>{},
-              std::integral_constant<int, (KG::SCH > 0 ? KG::SCH : 1)>{});
-    copy_part(rb + C::R_V, a.v_cache, a.v_bstride, 0, st, std::integral_constant<int, VG::ROW>{},
-              std::integral_constant<int, VG::CH>{});
-    copy_part(rb + C::R_VS, a.v_cache, a.v_bstride, a.v_dsec, st,
-              std::integral_constant<int, VG::SROW>{},
-              std::integral_constant<int, (VG::SCH > 0 ? VG::SCH : 1)>{});
-    if (tid < TOK) {
-      int64_t blk, rr;
-      vrow_s[b * TOK + tid] = row_src(st * TOK + tid, blk, rr) ? 1 : 0;
-    }
+    const int t = tid % TOK, part = tid / TOK;
+    int64_t blk = 0, rr = 0;
+    const bool ok = row_src(st * TOK + t, blk, rr);
+    const uint8_t* kb = a.k_cache + blk * a.k_bstride;
+    const uint8_t* vb = a.v_cache + blk * a.v_bstride;
+    copy_row(rb + t * KG::ROW, kb + rr * KG::ROW, a.k_cache, ok, part,
+             std::integral_constant<int, KG::ROW>{}, std::integral_constant<int, KG::CH>{});
+    copy_row(rb + C::R_KS + t * KG::SROW, kb + a.k_dsec + rr * KG::SROW, a.k_cache, ok, part,
+             std::integral_constant<int, KG::SROW>{}, std::integral_constant<int, (KG::SCH > 0 ? KG::SCH : 1)>{});
+    copy_row(rb + C::R_V + t * VG::ROW, vb + rr * VG::ROW, a.v_cache, ok, part,
+             std::integral_constant<int, VG::ROW>{}, std::integral_constant<int, VG::CH>{});
+    copy_row(rb + C::R_VS + t * VG::SROW, vb + a.v_dsec + rr * VG::SROW, a.v_cache, ok, part,
+             std::integral_constant<int, VG::SROW>{}, std::integral_constant<int, (VG::SCH > 0 ? VG::SCH : 1)>{});
+    if (part == 0) vrow_s[b * TOK + t] = ok ? 1 : 0;
   };
 
   t5::fence_before();
@@ -348,11 +352,11 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
   __syncthreads();
   if (st_begin < st_end) dequant_k(0);
   t5::fence_smem_async();
-  __syncthreads();
 
   for (int st = st_begin; st < st_end; ++st) {
     const int b = (st - st_begin) & 1;
     const uint32_t par = (uint32_t)((st - st_begin) & 1);
+    __syncthreads();   // K of step st in its plane; raw rows of step st visible
     // ---- S = Q . K^T (q hi x K hi, q lo x K hi, q hi x K lo)
     if (tid == 0) {
       t5::fence_after();
@@ -378,7 +382,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     if (!t5::wait(bar_s, par)) ok_all = false;
     t5::fence_after();
 
-    // ---- masked scores of this half row, row maximum through shared memory
+    // ---- this part of the score row, masked only where the step cuts a range
     static_assert(SC == 16, "one 16-column tensor-memory load per thread");
     float sv[SC];
     {
@@ -389,8 +393,6 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
       for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(v0[j]);
     }
     const int tbase = st * TOK + hf * SC;
-    // rows cut by the causal / window bounds, rows of the tile beyond its
-    // queries and invalid cache rows need the mask
     const uint32_t* vr4 = reinterpret_cast<const uint32_t*>(vrow_s + b * TOK + hf * SC);
     const bool full = row_ok && st * TOK >= all_lo && st * TOK + TOK - 1 <= all_hi &&
                       (vr4[0] & vr4[1] & vr4[2] & vr4[3]) == 0x01010101u;
@@ -409,7 +411,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
       }
     }
     mx_s[hf * C::ROWS + row] = mx;
-    if (!__syncthreads_and(ok_all)) break;   // also: V plane written by every thread
+    if (!__syncthreads_and(ok_all)) break;   // maxima and the V plane visible
 #pragma unroll
     for (int i = 0; i < NS; ++i) mx = fmaxf(mx, mx_s[i * C::ROWS + row]);
     float alpha = 1.f;
@@ -418,19 +420,20 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
       if (m_used == -CUDART_INF_F) {
         m_used = mx;
       } else if (mx > m_used + 8.f) {
-        alpha = exp2f(m_used - mx);
+        alpha = t5::ex2(m_used - mx);
         resc = true;
         l_sum *= alpha;
         m_used = mx;
       }
     }
+    const bool live = m_used != -CUDART_INF_F;   // else every score so far is masked: P = 0
 #pragma unroll
     for (int c8 = 0; c8 < SC; c8 += 8) {
       uint32_t h[4], l[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float x0 = sv[c8 + 2 * i] == -CUDART_INF_F ? 0.f : exp2f(sv[c8 + 2 * i] - m_used);
-        const float x1 = sv[c8 + 2 * i + 1] == -CUDART_INF_F ? 0.f : exp2f(sv[c8 + 2 * i + 1] - m_used);
+        const float x0 = live ? t5::ex2(sv[c8 + 2 * i] - m_used) : 0.f;
+        const float x1 = live ? t5::ex2(sv[c8 + 2 * i + 1] - m_used) : 0.f;
         l_sum += x0 + x1;
         tc::split2<VP::BF>(x0, x1, h[i], l[i]);
       }
@@ -451,9 +454,14 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
       }
       t5::wait_st();
     }
+    // raw rows two steps ahead into this step's buffer (its K and V are in
+    // their planes); those of the next step complete
+    if (st + 2 < st_end) issue(st + 2, b);
+    cp_async_commit();
+    cp_async_wait<1>();
     t5::fence_smem_async();
     t5::fence_before();
-    __syncthreads();
+    __syncthreads();   // P plane and the next step's raw rows visible
 
     // ---- O += P . V (P hi x V hi, P lo x V hi, P hi x V lo)
     if (tid == 0) {
@@ -472,16 +480,9 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
       }
       t5::commit(bar_o);
     }
-    // ---- meanwhile: raw rows two steps ahead, K of the next step
-    if (st + 2 < st_end) issue(st + 2, b);
-    cp_async_commit();
-    if (st + 1 < st_end) {
-      cp_async_wait<1>();
-      __syncthreads();   // raw rows of step st + 1 staged by every thread
-      dequant_k(b ^ 1);
-      t5::fence_smem_async();
-      __syncthreads();
-    }
+    // ---- meanwhile K of the next step (the K plane is free: S of this step is done)
+    if (st + 1 < st_end) dequant_k(b ^ 1);
+    t5::fence_smem_async();
   }
   cp_async_wait<0>();
   if (st_end > st_begin && ok_all) {
