@@ -148,3 +148,45 @@ def test_gemma_write_and_decode_full(fmt):
     assert np.array_equal(vc, vpool.cpu().numpy().reshape(-1))
     # decode over 16 x 8192 with 32 query heads
     _check(w, fmt, sampled=[5])
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "turbo4"])
+def test_prefill_full(fmt):
+    """The chunked-prefill workload at full size (8 x 4096 positions, the last
+    512 of every sequence the chunk, the launch bench.py times): queries of
+    two sampled sequences against the oracle, the first 8 and the last 8 of
+    each chunk (the first ones through the oracle's causal reading of a
+    shorter sequence)."""
+    w = W.make("prefill")
+    nq, nkv, hd, bs, C = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.chunk
+    sampled = [0, 5]
+    st = _fill(w, fmt, sampled)
+    kside, vside = oracle.kv_pair(fmt)
+    kst, vst = st["kpool"].stride(0), st["vpool"].stride(0)
+    kc = np.zeros(w.num_blocks * kst, np.uint8)
+    vc = np.zeros(w.num_blocks * vst, np.uint8)
+    for s in sampled:
+        n = st["lens"][s]
+        pos = np.arange(n)
+        slots = st["tables"][s, pos // bs].astype(np.int64) * bs + pos % bs
+        oracle.cache_write(kside, st["rows"][(s, 0)], kc, slots, nkv, hd, bs, kst, scale=st["k_scale"])
+        oracle.cache_write(vside, st["rows"][(s, 1)], vc, slots, nkv, hd, bs, vst, scale=st["v_scale"])
+    ns = len(st["lens"])
+    rng = np.random.default_rng(123)
+    q = bf16_round(rng.standard_normal((ns * C, nq, hd)).astype(np.float32))
+    cu = (np.arange(ns + 1) * C).astype(np.int32)
+    out = ops.paged_prefill(torch.from_numpy(q).to(DEV).to(torch.bfloat16), torch.from_numpy(cu).to(DEV), C,
+                            st["kpool"], st["vpool"], torch.from_numpy(st["tables"]).to(DEV),
+                            torch.from_numpy(np.asarray(st["lens"], np.int32)).to(DEV), fmt, nkv, bs,
+                            k_scale=st["k_scale"], v_scale=st["v_scale"])
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    k = 8
+    for s in sampled:
+        L = st["lens"][s]
+        tab = st["tables"][s:s + 1]
+        for first, Ls in ((C - k, L), (0, L - C + k)):   # last k queries, first k queries
+            qs = q[s * C + first:s * C + first + k]
+            ref = oracle.paged_prefill(qs, np.array([0, k]), kc, vc, tab, [Ls], nkv, hd, bs, kst, vst,
+                                       fmt, k_scale=st["k_scale"], v_scale=st["v_scale"])
+            assert_decode_close(got[s * C + first:s * C + first + k], ref)
