@@ -454,11 +454,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
       }
       t5::wait_st();
     }
-    // raw rows two steps ahead into this step's buffer (its K and V are in
-    // their planes); those of the next step complete
-    if (st + 2 < st_end) issue(st + 2, b);
-    cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<0>();   // the next step's raw rows (issued at the end of the previous step)
     t5::fence_smem_async();
     t5::fence_before();
     __syncthreads();   // P plane and the next step's raw rows visible
@@ -483,6 +479,11 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     // ---- meanwhile K of the next step (the K plane is free: S of this step is done)
     if (st + 1 < st_end) dequant_k(b ^ 1);
     t5::fence_smem_async();
+    // raw rows two steps ahead into this step's buffer (its K and V are in
+    // their planes), issued after this step's last proxy fence: a proxy fence
+    // also waits for the copies in flight (measured on GB300)
+    if (st + 2 < st_end) issue(st + 2, b);
+    cp_async_commit();
   }
   cp_async_wait<0>();
   if (st_end > st_begin && ok_all) {
