@@ -251,8 +251,9 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     rr = (int64_t)(pos & (a.bs - 1)) * a.nkv + kvh;
     return true;
   };
-  // Thread (row t = tid % TOK, part = tid / TOK) looks the row's block up
-  // once and copies chunks part, part + NT / TOK, ... of its four rows.
+  // Thread (row t = tid / PARTS, part = tid % PARTS) looks the row's block
+  // up once and copies chunks part, part + PARTS, ... of its four rows:
+  // consecutive threads write consecutive 16-byte chunks of one row.
   constexpr int PARTS = NT / TOK;
   auto copy_row = [&](uint8_t* dst, const uint8_t* src, const uint8_t* base, bool ok, int part,
                       auto rowbytes_c, auto chunk_c) {
@@ -267,7 +268,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     uint8_t* rb = raw + b * C::RAW;
     using KG = SideGeom<KS, HD>;
     using VG = SideGeom<VS, HD>;
-    const int t = tid % TOK, part = tid / TOK;
+    const int t = tid / PARTS, part = tid % PARTS;
     int64_t blk = 0, rr = 0;
     const bool ok = row_src(st * TOK + t, blk, rr);
     const uint8_t* kb = a.k_cache + blk * a.k_bstride;
