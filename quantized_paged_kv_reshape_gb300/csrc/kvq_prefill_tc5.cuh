@@ -126,6 +126,57 @@ __device__ __forceinline__ int cm(int r, int k) {
 
 }  // namespace t5
 
+// Codebook sides (Turbo2/3/4, NVFP4): a table of code pairs, entry
+// (c0 | c1 << bits) = fp16x2 (hi(c0), hi(c1)) and (lo(c0), lo(c1)) with the
+// level split into two parts of 7 significant bits, PCOPY copies
+// interleaved against bank conflicts.  A part times an E4M3 group scale (4
+// significant bits) is exact in fp16.
+constexpr int PCOPY = 4;
+template <int S>
+constexpr int pair_entries() { return side_codebook(S) ? (1 << (2 * code_bits(S))) * PCOPY : 0; }
+
+template <int S>
+__device__ __forceinline__ void t5_fill_pairs(uint2* lut, const Codebooks& cb, int tid, int nt) {
+  if constexpr (side_codebook(S)) {
+    const float* lv = side_levels<S>(cb);
+    constexpr int B = code_bits(S), n = 1 << B;
+    for (int e = tid; e < pair_entries<S>(); e += nt) {
+      const int pr = e / PCOPY;
+      const float c0 = lv[pr & (n - 1)], c1 = lv[pr >> B];
+      const float h0 = tc::round_sig7(c0), h1 = tc::round_sig7(c1);
+      const float l0 = tc::round_sig7(c0 - h0), l1 = tc::round_sig7(c1 - h1);
+      lut[e] = make_uint2(tc::pack2<false>(h0, h1), tc::pack2<false>(l0, l1));
+    }
+  }
+}
+
+// Elements d0 .. d0 + 7 (d0 % 8 == 0, one scale group) of a staged codebook
+// row as fp16x2 hi / lo pairs: one table entry per code pair, scaled in fp16.
+template <int S>
+__device__ __forceinline__ void t5_dequant_pairs(const uint8_t* row, const uint8_t* srow, int d0,
+                                                 const uint2* lut, int cpy, uint32_t (&hw)[4],
+                                                 uint32_t (&lw)[4]) {
+  constexpr int B = code_bits(S);
+  uint32_t w;
+  if constexpr (B == 4) {
+    w = *reinterpret_cast<const uint32_t*>(row + d0 / 2);
+  } else if constexpr (B == 2) {
+    w = *reinterpret_cast<const uint16_t*>(row + d0 / 4);
+  } else {   // 3-bit codes: 24 bits from byte 3 d0 / 8
+    const uint8_t* p = row + 3 * (d0 / 8);
+    w = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16);
+  }
+  const uint32_t sb = srow[d0 / kGroup];
+  const uint32_t sc2 = tc::e4m3x2_f16x2(sb | (sb << 8));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t pr = (w >> (2 * B * i)) & ((1u << (2 * B)) - 1u);
+    const uint2 e = lut[pr * PCOPY + cpy];
+    hw[i] = tc::hmul2(e.x, sc2);
+    lw[i] = PfSide<S>::PLANES == 2 ? tc::hmul2(e.y, sc2) : 0u;
+  }
+}
+
 template <int KS, int VS, int HD>
 struct T5Cfg {
   static_assert(HD == 64 || HD == 128, "tensor-memory prefill: head_dim 64 or 128");
@@ -146,7 +197,10 @@ struct T5Cfg {
   static constexpr int OFF_RAW = OFF_P + 2 * PB;      // raw rows, two buffers
   static constexpr int OFF_VROW = OFF_RAW + 2 * RAW;  // [2][TOK] row valid flags
   static constexpr int OFF_LV = OFF_VROW + 2 * TOK;   // level tables [2][2][16] fp32
-  static constexpr int OFF_MX = OFF_LV + 256;         // [NSPLIT][ROWS] part-row maxima / sums
+  static constexpr bool SHARE_PAIRS = KS == VS;
+  static constexpr int OFF_PK = OFF_LV + 256;          // code-pair tables (K, then V unless shared)
+  static constexpr int OFF_PV = OFF_PK + (SHARE_PAIRS ? 0 : pair_entries<KS>() * 8);
+  static constexpr int OFF_MX = OFF_PV + pair_entries<VS>() * 8;  // [NSPLIT][ROWS] part-row maxima / sums
   static constexpr int OFF_BAR = OFF_MX + NSPLIT * ROWS * 4;  // 2 mbarriers, tensor-memory address
   static constexpr int SMEM_MAIN = OFF_BAR + 32;
   static constexpr int OUTB = ROWS * (HD + 4) * 4;    // output staging (fp32), reuses the planes
@@ -237,6 +291,10 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
   }
   pf_fill_levels<KS>(lv, lv + 16, cb, tid, NT);
   pf_fill_levels<VS>(lv + 32, lv + 48, cb, tid, NT);
+  const uint2* pk = reinterpret_cast<const uint2*>(smem + C::OFF_PK);
+  const uint2* pv = reinterpret_cast<const uint2*>(smem + C::OFF_PV);
+  t5_fill_pairs<KS>(reinterpret_cast<uint2*>(smem + C::OFF_PK), cb, tid, NT);
+  if constexpr (!C::SHARE_PAIRS) t5_fill_pairs<VS>(reinterpret_cast<uint2*>(smem + C::OFF_PV), cb, tid, NT);
 
   const int p_first = max(pbase, 0);
   const int lo_first = a.window > 0 ? max(0, p_first + 1 - a.window) : 0;
@@ -311,7 +369,10 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     for (int q = tid; q < TOK * (HD / 8); q += NT) {
       const int t = q / (HD / 8), d0 = (q % (HD / 8)) * 8;
       uint32_t hw[4], lw[4];
-      pf_dequant<KS, HD, 8>(rb + t * C::KROW, rb + C::R_KS + t * C::KSROW, d0, lv, lv + 16, hw, lw);
+      if constexpr (side_codebook(KS))
+        t5_dequant_pairs<KS>(rb + t * C::KROW, rb + C::R_KS + t * C::KSROW, d0, pk, tid & (PCOPY - 1), hw, lw);
+      else
+        pf_dequant<KS, HD, 8>(rb + t * C::KROW, rb + C::R_KS + t * C::KSROW, d0, lv, lv + 16, hw, lw);
       const int o_ = t5::cm<HD>(t, d0);
       *reinterpret_cast<uint4*>(k_s + o_) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       if constexpr (C::KPL == 2)
@@ -326,8 +387,12 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
       uint32_t vh[4][4], vl[4][4];
 #pragma unroll
       for (int t = 0; t < 4; ++t)
-        pf_dequant<VS, HD, 8>(rb + C::R_V + (tb + t) * C::VROW, rb + C::R_VS + (tb + t) * C::VSROW, d0,
-                              lv + 32, lv + 48, vh[t], vl[t]);
+        if constexpr (side_codebook(VS))
+          t5_dequant_pairs<VS>(rb + C::R_V + (tb + t) * C::VROW, rb + C::R_VS + (tb + t) * C::VSROW, d0, pv,
+                               tid & (PCOPY - 1), vh[t], vl[t]);
+        else
+          pf_dequant<VS, HD, 8>(rb + C::R_V + (tb + t) * C::VROW, rb + C::R_VS + (tb + t) * C::VSROW, d0,
+                                lv + 32, lv + 48, vh[t], vl[t]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {   // dims d0 + 2i, d0 + 2i + 1 over the 4 tokens
         *reinterpret_cast<uint2*>(v_s + t5::cm<TOK>(d0 + 2 * i, tb)) =
