@@ -61,6 +61,15 @@ TRAFFIC = {
     ("llama8b", "fp8"): 273_162_240,
     ("llama8b", "turbo4"): 156_372_992,
 }
+# smsp__inst_executed.sum per launch (warp-instructions) of the same capture:
+# the second roofline of the decode formats that are issue bound.  Issue
+# peak = 4 warp-instructions per cycle per SM (one per sub-partition) x the
+# SMs x the SM clock sampled during the timed region.
+WARP_INSTR = {
+    ("llama8b", "bf16"): 25_284_741,
+    ("llama8b", "fp8"): 28_836_709,
+    ("llama8b", "turbo4"): 64_875_461,
+}
 
 
 def peaks():
@@ -385,6 +394,18 @@ def run_gpu(args):
         key = f if len(windows) == 1 else f"{f}@window{win}"
         per_layer[key] = {"us_per_layer": round(us, 2), "decode_gbs": round(gbs, 1),
                           "frac_of_peak": round(gbs / peak, 4), "cache_bytes": dec_bytes[(f, win)]}
+    full_size = not args.num_seqs or args.num_seqs == W.make(args.workload).num_seqs
+    sm_hz = (clocks or {}).get("sm_mhz") or 0.0
+    if full_size and sm_hz:
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        issue_peak = 4.0 * nsm * sm_hz * 1e6
+        for key, d in per_layer.items():
+            n = WARP_INSTR.get((args.workload, key))
+            if n:
+                rate = n / (d["us_per_layer"] * 1e-6)
+                d["issue"] = {"warp_instr": n, "achieved_ginst_s": round(rate / 1e9, 1),
+                              "peak_ginst_s": round(issue_peak / 1e9, 1),
+                              "frac": round(rate / issue_peak, 4)}
     per_write = {}
     for f in fmts:
         wms = statistics.mean(write_ms[f])
@@ -398,7 +419,7 @@ def run_gpu(args):
     e2e_value = job_rate(step_bytes, ws, e2e_ms)
     launches_per_step = len(fmts) * ((2 if prefill is not None else 1) + len(windows))
     dom_fmt = dom.split("@")[0]
-    traffic = TRAFFIC.get((args.workload, dom)) if not args.num_seqs or args.num_seqs == W.make(args.workload).num_seqs else None
+    traffic = TRAFFIC.get((args.workload, dom)) if full_size else None
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
