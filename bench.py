@@ -175,6 +175,59 @@ def write_bytes(fmt, ntok, nkv, hd, bs, in_bytes=2):
 
 # --------------------------------------------------------------------- GPU arm
 
+def _compare(got, ref):
+    """max / mean |got - ref| and the cosine of each (sequence, head) output
+    row with its reference row (rows whose reference is zero are skipped)."""
+    d = (got - ref).abs()
+    g2, r2 = got.reshape(-1, got.shape[-1]).double(), ref.reshape(-1, ref.shape[-1]).double()
+    nr = r2.norm(dim=1)
+    keep = nr > 0
+    cos = (g2 * r2).sum(dim=1)[keep] / (g2.norm(dim=1)[keep] * nr[keep]).clamp_min(1e-300)
+    return {"max_abs": float(d.max()), "mean_abs": float(d.mean()),
+            "cos_min": round(float(cos.min()), 6) if cos.numel() else None,
+            "cos_mean": round(float(cos.mean()), 6) if cos.numel() else None}
+
+
+def quality_report(ops, torch, ref_pools, pools, fmts, windows, q, tables, lens, nkv, bs, nseq,
+                   nq, hd, mb, k_scale, v_scale, wsp, in_dtype, dev, sparse=1e-3, reps=10):
+    """Decode output of each format against the BF16-cache decode of the same
+    K/V (unquantized attention; that kernel is within 2e-3 / 2e-4 of the fp64
+    oracle in the parity tests), exact and with the sparse-V skip (weights
+    <= 1e-3 of the running sum dropped), and the sparse-V decode time."""
+    rkp, rvp = ref_pools
+    rep = {"reference": "bf16-cache decode of the same K/V"
+                        + ("" if in_dtype == "bf16" else " (inputs rounded to bf16)"),
+           "sparse_v_threshold": sparse}
+    stream = torch.cuda.current_stream()
+    for win in windows:
+        rws = ops.alloc_workspace(nseq, nq, nkv, hd, bs, mb, win, "bf16", device=dev)
+        ref = ops.paged_decode(q, rkp, rvp, tables, lens, "bf16", nkv, bs, sliding_window=win,
+                               workspace=rws)
+        for f in fmts:
+            kp, vp = pools[f]
+
+            def dec(thr, f=f, kp=kp, vp=vp, win=win):
+                return ops.paged_decode(q, kp, vp, tables, lens, f, nkv, bs, k_scale=k_scale,
+                                        v_scale=v_scale, sliding_window=win,
+                                        sparse_v_threshold=thr, workspace=wsp[(f, win)])
+            exact = dec(0.0)
+            sp = dec(sparse)
+            dec(sparse)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for e0, e1 in evs:
+                e0.record(stream)
+                dec(sparse)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+            key = f if len(windows) == 1 else f"{f}@window{win}"
+            rep[key] = {"exact": _compare(exact, ref),
+                        "sparse_v": dict(_compare(sp, ref), vs_exact=_compare(sp, exact),
+                                         us_per_layer=round(us, 2))}
+    return rep
+
+
 def run_gpu(args):
     import torch
     from quantized_paged_kv_reshape_gb300 import ops, workloads as W
@@ -251,6 +304,15 @@ def run_gpu(args):
     outs = {f: torch.empty((nseq, nq, hd), dtype=torch.float32, device=dev) for f in fmts}
     wsp = {(f, win): ops.alloc_workspace(nseq, nq, nkv, hd, bs, mb, win, f, device=dev)
            for f in fmts for win in windows}
+    # Unquantized reference for the quality report: a BF16 cache of the same
+    # K/V (the workload's inputs are bf16, so this cache holds them exactly).
+    ref_pools = None
+    if not args.no_quality:
+        rkp = ops.alloc_pool(w.num_blocks, "bf16", 0, bs, nkv, hd, device=dev)
+        rvp = ops.alloc_pool(w.num_blocks, "bf16", 1, bs, nkv, hd, device=dev)
+        ops.cache_write(kall.view(ntok, -1), vall.view(ntok, -1), rkp, rvp, slots_all, "bf16",
+                        nkv, hd, bs)
+        ref_pools = (rkp, rvp)
     del kall, vall
 
     stream = torch.cuda.current_stream()
@@ -380,6 +442,9 @@ def run_gpu(args):
     e2e_ms = s0.elapsed_time(s1) / e_steps
 
     ms_step, e2e_ms = slowest_rank([ms_total / args.steps, e2e_ms], dev)
+    quality = quality_report(ops, torch, ref_pools, pools, fmts, windows, q, tables, lens, nkv,
+                             bs, nseq, nq, hd, mb, k_scale, v_scale, wsp, w.in_dtype, dev) \
+        if ref_pools is not None else None
 
     dec_bytes = {(f, win): algorithmic_decode_bytes(f, w.seq_lens, nkv, hd, bs, win)
                  for f in fmts for win in windows}
@@ -442,6 +507,8 @@ def run_gpu(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if quality is not None:
+        line["quality"] = quality
     if ws > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -657,6 +724,8 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-quality", action="store_true",
+                    help="skip the quality report against a BF16 cache of the same K/V")
     ap.add_argument("--graphs", action="store_true",
                     help="time per-call CUDA graph replays instead of direct calls")
     ap.add_argument("--num-seqs", type=int, default=0, help="override the number of sequences")

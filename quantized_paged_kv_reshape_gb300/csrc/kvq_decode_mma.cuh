@@ -957,6 +957,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
         l1 = l1 * al1 + (pw[0][1] + pw[0][3]) + (pw[1][1] + pw[1][3]);
         m0 = mn0;
         m1 = mn1;
+        bool pv_any = true;
         if (a.sparse_thr > 0.f) {  // drop weights <= thr x (this warp's running sum)
           float t0 = l0, t1 = l1;
 #pragma unroll
@@ -964,13 +965,18 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
             t0 += __shfl_xor_sync(0xffffffffu, t0, msk);
             t1 += __shfl_xor_sync(0xffffffffu, t1, msk);
           }
+          bool nz = false;
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
             if (pw[h][0] <= a.sparse_thr * t0) pw[h][0] = 0.f;
             if (pw[h][2] <= a.sparse_thr * t0) pw[h][2] = 0.f;
             if (pw[h][1] <= a.sparse_thr * t1) pw[h][1] = 0.f;
             if (pw[h][3] <= a.sparse_thr * t1) pw[h][3] = 0.f;
+            nz = nz || pw[h][0] != 0.f || pw[h][1] != 0.f || pw[h][2] != 0.f || pw[h][3] != 0.f;
           }
+          // a slab whose weights were all dropped skips its V dequantization
+          // and P.V products (the skip the threshold exists for)
+          pv_any = __any_sync(0xffffffffu, nz);
         }
         if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
@@ -978,10 +984,12 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
             o[i][0] *= al0; o[i][1] *= al1; o[i][2] *= al0; o[i][3] *= al1;
           }
         }
+        if (pv_any) {
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
-          pv16(sb + C::OFF_V + 16 * h * VT::VRS, sb + C::OFF_VS + 16 * h * VT::SROW, pw[h][0],
-               pw[h][1], pw[h][2], pw[h][3]);
+          for (int h = 0; h < NH; ++h)
+            pv16(sb + C::OFF_V + 16 * h * VT::VRS, sb + C::OFF_VS + 16 * h * VT::SROW, pw[h][0],
+                 pw[h][1], pw[h][2], pw[h][3]);
+        }
       }
       cp_async_wait<0>();
     }
