@@ -57,18 +57,18 @@ WORKLOAD_DESC = {
 # decode launch, from the ncu capture summarised in profiles/ (None when the
 # kernel changed after the capture).
 TRAFFIC = {
-    ("llama8b", "bf16"): 541_731_328,
-    ("llama8b", "fp8"): 273_162_240,
-    ("llama8b", "turbo4"): 156_372_992,
+    ("llama8b", "bf16"): 541_566_720,
+    ("llama8b", "fp8"): 270_267_136,
+    ("llama8b", "turbo4"): 152_794_624,
 }
 # smsp__inst_executed.sum per launch (warp-instructions) of the same capture:
 # the second roofline of the decode formats that are issue bound.  Issue
 # peak = 4 warp-instructions per cycle per SM (one per sub-partition) x the
 # SMs x the SM clock sampled during the timed region.
 WARP_INSTR = {
-    ("llama8b", "bf16"): 25_284_741,
-    ("llama8b", "fp8"): 28_836_709,
-    ("llama8b", "turbo4"): 64_875_461,
+    ("llama8b", "bf16"): 25_479_173,
+    ("llama8b", "fp8"): 29_086_821,
+    ("llama8b", "turbo4"): 65_006_533,
 }
 
 
