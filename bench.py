@@ -52,6 +52,9 @@ WORKLOAD_DESC = {
     "tiny": "tiny: {nseq} seqs of 37/50 tokens, 4 q / 2 kv heads, head_dim 64",
     "prefill": "chunked prefill layer: {nseq} seqs x 4096 ctx, last 512 positions the new chunk "
                "(written, then attended causally), 32 q / 8 kv heads, head_dim 128, block_size 16",
+    "prefill_hd256": "chunked prefill layer: {nseq} seqs x 4096 ctx, last 512 positions the new "
+                     "chunk (written, then attended causally), 32 q / 16 kv heads, head_dim 256, "
+                     "block_size 16",
 }
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # decode launch, from the ncu capture summarised in profiles/ (None when the
@@ -589,7 +592,7 @@ def run_prefill(args):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     _abi.lib()
-    w = W.make("prefill", seed=rank)
+    w = W.make(args.workload, seed=rank)
     nkv, nq, hd, bs, C = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size, w.chunk
     nseq = w.num_seqs
     lens_np = np.asarray(w.seq_lens, np.int64)
@@ -679,7 +682,7 @@ def run_prefill(args):
             "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16/bf16 hi+lo operands, f32 accumulate",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC["prefill"].format(nseq=nseq), "formats": fmts,
+            "config": {"workload": WORKLOAD_DESC[args.workload].format(nseq=nseq), "formats": fmts,
                        "l2": "caches far above L2 between steps",
                        "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
             "per_layer": per_layer,
@@ -736,7 +739,7 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload == "prefill":
+    elif args.workload.startswith("prefill"):
         run_prefill(args)
     else:
         run_gpu(args)

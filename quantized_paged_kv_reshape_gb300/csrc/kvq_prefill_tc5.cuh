@@ -1,30 +1,33 @@
 // Chunked-prefill attention on the 5th-generation tensor cores (tcgen05,
-// accumulators in tensor memory), head_dim 64 and 128.
+// accumulators in tensor memory), head_dim 64, 128 and 256.
 //
-// Same result as prefill_tc_kernel ("combs_models/kv.rs" attend with the
-// causal / window mask and repeat_kv, "spark_runtime/kv_cache.rs"
-// is_wht_rotated bookends): query i of sequence s's chunk sits at
-// p = L - C + i and attends to [max(0, p + 1 - W), p].
+// "combs_models/kv.rs" attend with the causal / window mask and repeat_kv,
+// "spark_runtime/kv_cache.rs" is_wht_rotated bookends: query i of sequence
+// s's chunk sits at p = L - C + i and attends to [max(0, p + 1 - W), p].
 //
-// One CTA (16 warps) per (tile of 128 score rows = QT query tokens x RP
-// heads, kv head, sequence); score row r is tensor-memory lane r, held by
-// threads r + 128 i, i = 0..3, each with a quarter of its columns.  Per step
-// of 64 KV positions (raw cache rows staged by cp.async two steps ahead):
-//   one thread issues S[128 x 64] = Q . K^T (tcgen05.mma kind::f16, fp32 in
+// One CTA (16 warps) per (tile of R score rows = QT query tokens x RP
+// heads, kv head, sequence), R = 128 for head_dim 64/128 and R = 64 for
+// head_dim 256 (whose planes would not fit a 128-row tile).  With R = 128
+// score row r is tensor-memory lane r, held by threads r + 128 i, i = 0..3,
+// each with a quarter of its columns; with R = 64 (M = 64 accumulators) row
+// r sits in lane 32 floor(r / 16) + r mod 16, so the first 16 lanes of each
+// warp hold rows.  Per step of T KV positions (T = 64, or 32 for head_dim
+// 256; raw cache rows staged by cp.async two steps ahead):
+//   one thread issues S[R x T] = Q . K^T (tcgen05.mma kind::f16, fp32 in
 //   tensor memory; K dequantized during the previous step) and commits it
 //   to an mbarrier;
-//   meanwhile all threads dequantize V into the V^T [hd x 64] operand plane
+//   meanwhile all threads dequantize V into the V^T [hd x T] operand plane
 //   (16-bit hi + lo parts where one 16-bit value is not exact);
 //   each thread reads its quarter score row (tcgen05.ld), masks it (only on
 //   steps that cut a row's range); the quarters' maxima meet in shared
-//   memory; it writes its quarter P row (hi + lo)
-//   to shared memory; the O accumulator in tensor memory is rescaled only
-//   when a row's maximum grew by more than 2^8 since the last rescale (P <=
-//   2^8 otherwise: exact enough in fp32 and in the 16-bit parts);
-//   one thread issues O[128 x hd] += P . V, and meanwhile all threads
-//   dequantize the next step's K into the K [64 x hd] plane.
+//   memory; it writes its quarter P row (hi + lo) to shared memory; the O
+//   accumulator in tensor memory is rescaled only when a row's maximum grew
+//   by more than 2^8 since the last rescale (P <= 2^8 otherwise: exact
+//   enough in fp32 and in the 16-bit parts);
+//   one thread issues O[R x hd] += P . V, and meanwhile all threads
+//   dequantize the next step's K into the K [T x hd] plane.
 // q (scaled by the score scale) and P carry hi + lo 16-bit parts like the
-// mma.sync kernels.  Operands are K-major without swizzle (8 x 16-byte core
+// decode.  Operands are K-major without swizzle (8 x 16-byte core
 // matrices; strides in t5::cm).
 #pragma once
 
@@ -92,6 +95,12 @@ __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&v)[16]) {
         "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
         "=r"(v[15])
       : "r"(taddr));
+}
+__device__ __forceinline__ void ld8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                 "=r"(v[7])
+               : "r"(taddr));
 }
 __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
@@ -179,8 +188,13 @@ __device__ __forceinline__ void t5_dequant_pairs(const uint8_t* row, const uint8
 
 template <int KS, int VS, int HD>
 struct T5Cfg {
-  static_assert(HD == 64 || HD == 128, "tensor-memory prefill: head_dim 64 or 128");
-  static constexpr int NT = 512, ROWS = 128, TOK = 64, NSPLIT = NT / ROWS;
+  static_assert(HD == 64 || HD == 128 || HD == 256, "tensor-memory prefill: head_dim 64, 128 or 256");
+  // M of the accumulators (score rows per tile) and KV positions per step;
+  // NSPLIT column parts per row (the four warps of a lane quadrant)
+  static constexpr int NT = 512, ROWS = HD == 256 ? 64 : 128, TOK = HD == 256 ? 32 : 64, NSPLIT = 4;
+  // tokens per V dequantization item (head_dim 256: 2, so that 32-position
+  // steps still give every thread an item)
+  static constexpr int VTPI = HD == 256 ? 2 : 4;
   static constexpr int KPL = PfSide<KS>::PLANES, VPL = PfSide<VS>::PLANES;
   static constexpr int KROW = SideGeom<KS, HD>::ROW, KSROW = SideGeom<KS, HD>::SROW;
   static constexpr int VROW = SideGeom<VS, HD>::ROW, VSROW = SideGeom<VS, HD>::SROW;
@@ -206,7 +220,7 @@ struct T5Cfg {
   static constexpr int OUTB = ROWS * (HD + 4) * 4;    // output staging (fp32), reuses the planes
   static constexpr int SMEM = SMEM_MAIN > OUTB ? SMEM_MAIN : OUTB;
   static constexpr int S_COL = 0, O_COL = TOK;         // tensor-memory columns of S and O
-  static constexpr int TCOLS = TOK + HD <= 128 ? 128 : 256;
+  static constexpr int TCOLS = TOK + HD <= 128 ? 128 : TOK + HD <= 256 ? 256 : 512;
 };
 
 template <int KS, int VS, int HD>
@@ -347,14 +361,20 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
   t5::fence_after();
   const uint32_t tmem = *tslot;
   constexpr int NS = C::NSPLIT, SC = TOK / NS, OC = HD / NS;   // columns per thread of S, of O
-  const int row = tid & (C::ROWS - 1), hf = tid >> 7;          // score row, column part
+  constexpr bool M64 = C::ROWS == 64;
+  // score row and column part: lane 32 (warp & 3) + lane of tensor memory
+  // holds row 32 (warp & 3) + lane (M = 128), or row 16 (warp & 3) + lane
+  // for lanes 0-15 (M = 64; lanes 16-31 hold no row)
+  const bool has_row = !M64 || lane < 16;
+  const int row = M64 ? 16 * (warp & 3) + (lane & 15) : tid & (C::ROWS - 1);
+  const int hf = warp >> 2;
   const uint32_t t_lane = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's lanes (rows)
   const uint32_t s_tm = tmem + C::S_COL + hf * SC, o_tm = tmem + C::O_COL;
   float* mx_s = reinterpret_cast<float*>(smem + C::OFF_MX);    // [NS][ROWS]
 
   // per-row softmax state (both threads of a row keep the same m_used)
   const int qi_r = row / rp, hj_r = row - qi_r * rp;
-  const bool row_ok = qi_r < nq_tile && hj_r < a.rep;
+  const bool row_ok = has_row && qi_r < nq_tile && hj_r < a.rep;
   const int p_r = pbase + qi_r;
   const int lo_r = a.window > 0 ? p_r + 1 - a.window : 0;
   float m_used = -CUDART_INF_F, l_sum = 0.f;
@@ -379,20 +399,34 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
         *reinterpret_cast<uint4*>(k_s + C::KB / 2 + o_) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
   };
-  // V of a staged step into the V^T plane: thread = 4 tokens x 8 dims.
+  // V of a staged step into the V^T plane: thread = VTPI tokens x 8 dims.
+  constexpr int VT = C::VTPI;
   auto dequant_v = [&](int b) {
     const uint8_t* rb = raw + b * C::RAW;
-    for (int q = tid; q < (TOK / 4) * (HD / 8); q += NT) {
-      const int tb = (q / (HD / 8)) * 4, d0 = (q % (HD / 8)) * 8;
-      uint32_t vh[4][4], vl[4][4];
+    for (int q = tid; q < (TOK / VT) * (HD / 8); q += NT) {
+      const int tb = (q / (HD / 8)) * VT, d0 = (q % (HD / 8)) * 8;
+      uint32_t vh[VT][4], vl[VT][4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
+      for (int t = 0; t < VT; ++t)
         if constexpr (side_codebook(VS))
           t5_dequant_pairs<VS>(rb + C::R_V + (tb + t) * C::VROW, rb + C::R_VS + (tb + t) * C::VSROW, d0, pv,
                                tid & (PCOPY - 1), vh[t], vl[t]);
         else
           pf_dequant<VS, HD, 8>(rb + C::R_V + (tb + t) * C::VROW, rb + C::R_VS + (tb + t) * C::VSROW, d0,
                                 lv + 32, lv + 48, vh[t], vl[t]);
+      if constexpr (VT == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // dims d0 + 2i, d0 + 2i + 1 over the 2 tokens
+          *reinterpret_cast<uint32_t*>(v_s + t5::cm<TOK>(d0 + 2 * i, tb)) = tc::prmt(vh[0][i], vh[1][i], 0x5410u);
+          *reinterpret_cast<uint32_t*>(v_s + t5::cm<TOK>(d0 + 2 * i + 1, tb)) = tc::prmt(vh[0][i], vh[1][i], 0x7632u);
+          if constexpr (C::VPL == 2) {
+            *reinterpret_cast<uint32_t*>(v_s + C::VB / 2 + t5::cm<TOK>(d0 + 2 * i, tb)) =
+                tc::prmt(vl[0][i], vl[1][i], 0x5410u);
+            *reinterpret_cast<uint32_t*>(v_s + C::VB / 2 + t5::cm<TOK>(d0 + 2 * i + 1, tb)) =
+                tc::prmt(vl[0][i], vl[1][i], 0x7632u);
+          }
+        }
+      } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {   // dims d0 + 2i, d0 + 2i + 1 over the 4 tokens
         *reinterpret_cast<uint2*>(v_s + t5::cm<TOK>(d0 + 2 * i, tb)) =
@@ -405,6 +439,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
           *reinterpret_cast<uint2*>(v_s + C::VB / 2 + t5::cm<TOK>(d0 + 2 * i + 1, tb)) =
               make_uint2(tc::prmt(vl[0][i], vl[1][i], 0x7632u), tc::prmt(vl[2][i], vl[3][i], 0x7632u));
         }
+      }
       }
     }
   };
@@ -426,7 +461,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     // ---- S = Q . K^T (q hi x K hi, q lo x K hi, q hi x K lo)
     if (tid == 0) {
       t5::fence_after();
-      constexpr uint32_t ID = t5::idesc(KP::BF, 128, TOK);
+      constexpr uint32_t ID = t5::idesc(KP::BF, C::ROWS, TOK);
       constexpr uint32_t SBO = t5::sbo<HD>(), KSTEP = 2 * t5::kLbo;
       const uint32_t qa = t5::smem_addr(qh_s), qb = t5::smem_addr(ql_s), ka = t5::smem_addr(k_s);
 #pragma unroll
@@ -449,19 +484,23 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     t5::fence_after();
 
     // ---- this part of the score row, masked only where the step cuts a range
-    static_assert(SC == 16, "one 16-column tensor-memory load per thread");
+    static_assert(SC == 16 || SC == 8, "one tensor-memory load per thread");
     float sv[SC];
     {
-      uint32_t v0[16];
-      t5::ld16(s_tm + t_lane, v0);
+      uint32_t v0[SC];
+      if constexpr (SC == 16) t5::ld16(s_tm + t_lane, v0);
+      else t5::ld8(s_tm + t_lane, v0);
       t5::wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(v0[j]);
+      for (int j = 0; j < SC; ++j) sv[j] = __uint_as_float(v0[j]);
     }
     const int tbase = st * TOK + hf * SC;
     const uint32_t* vr4 = reinterpret_cast<const uint32_t*>(vrow_s + b * TOK + hf * SC);
+    uint32_t vand = 0x01010101u;
+#pragma unroll
+    for (int w4 = 0; w4 < SC / 4; ++w4) vand &= vr4[w4];
     const bool full = row_ok && st * TOK >= all_lo && st * TOK + TOK - 1 <= all_hi &&
-                      (vr4[0] & vr4[1] & vr4[2] & vr4[3]) == 0x01010101u;
+                      vand == 0x01010101u;
     float mx = -CUDART_INF_F;
     if (full) {
 #pragma unroll
@@ -476,7 +515,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
         mx = fmaxf(mx, sv[j]);
       }
     }
-    mx_s[hf * C::ROWS + row] = mx;
+    if (has_row) mx_s[hf * C::ROWS + row] = mx;
     if (!__syncthreads_and(ok_all)) break;   // maxima and the V plane visible
 #pragma unroll
     for (int i = 0; i < NS; ++i) mx = fmaxf(mx, mx_s[i * C::ROWS + row]);
@@ -504,8 +543,10 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
         tc::split2<VP::BF>(x0, x1, h[i], l[i]);
       }
       const int o_ = t5::cm<TOK>(row, hf * SC + c8);
-      *reinterpret_cast<uint4*>(ph_s + o_) = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(pl_s + o_) = make_uint4(l[0], l[1], l[2], l[3]);
+      if (has_row) {
+        *reinterpret_cast<uint4*>(ph_s + o_) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(pl_s + o_) = make_uint4(l[0], l[1], l[2], l[3]);
+      }
     }
     // rescale this part of the O rows whose maximum grew (warp-collective accesses)
     if (st > st_begin && __any_sync(0xffffffffu, resc)) {
@@ -528,7 +569,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     // ---- O += P . V (P hi x V hi, P lo x V hi, P hi x V lo)
     if (tid == 0) {
       t5::fence_after();
-      constexpr uint32_t ID = t5::idesc(VP::BF, 128, HD);
+      constexpr uint32_t ID = t5::idesc(VP::BF, C::ROWS, HD);
       constexpr uint32_t SBO = t5::sbo<TOK>(), KSTEP = 2 * t5::kLbo;
       const uint32_t pa = t5::smem_addr(ph_s), pb = t5::smem_addr(pl_s), va = t5::smem_addr(v_s);
 #pragma unroll
@@ -557,7 +598,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
   }
   if (!ok_all && tid == 0 && a.err) atomicOr(a.err, 4);
   t5::fence_after();
-  mx_s[hf * C::ROWS + row] = l_sum;
+  if (has_row) mx_s[hf * C::ROWS + row] = l_sum;
   __syncthreads();   // every plane read is done: the output staging reuses them
   l_sum = 0.f;
 #pragma unroll
@@ -576,8 +617,10 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
         t5::ld16(o_tm + t_lane + c0, v);
         t5::wait_ld();
       }
+      if (has_row) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) os[row * (HD + 4) + c0 + j] = have_o ? __uint_as_float(v[j]) * inv : 0.f;
+        for (int j = 0; j < 16; ++j) os[row * (HD + 4) + c0 + j] = have_o ? __uint_as_float(v[j]) * inv : 0.f;
+      }
     }
   }
   t5::fence_before();
@@ -615,15 +658,13 @@ cudaError_t launch_prefill_tc5(const PrefillArgs& a, const Codebooks& cb, int ma
   return cudaGetLastError();
 }
 
-// head_dim 64 and 128 run on tcgen05; head_dim 256 (whose operand planes do
-// not fit the shared memory of a 128-row tile) on the mma.sync kernel.
 template <int KS, int VS>
 cudaError_t launch_prefill_pair(int hd, const PrefillArgs& a, const Codebooks& cb, int max_chunk,
                                 cudaStream_t st) {
   switch (hd) {
     case 64: return launch_prefill_tc5<KS, VS, 64>(a, cb, max_chunk, st);
     case 128: return launch_prefill_tc5<KS, VS, 128>(a, cb, max_chunk, st);
-    case 256: return launch_prefill_inst<KS, VS, 256>(a, cb, max_chunk, st);
+    case 256: return launch_prefill_tc5<KS, VS, 256>(a, cb, max_chunk, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -30,6 +30,9 @@ Workloads (sizes follow the quantized-KV-cache pages' use cases):
   positions whose last 512 are the new chunk (written, then attended
   causally), 32 query / 8 KV heads, head_dim 128, llama8b's value
   distribution; formats bf16, fp8, turbo4.
+* ``prefill_hd256``: the same chunked prefill, Gemma-shaped: 32 query / 16 KV
+  heads, head_dim 256, K and V N(0,1) bf16 as gemma_write; formats bf16,
+  turbo2, turbo8.
 
 Block tables are seeded permutations of the physical block ids, sliced per
 sequence, so no two sequences share a block.
@@ -100,6 +103,9 @@ def make(name, seed=0, **over):
     elif name == "prefill":
         w = Workload("prefill", 8, np.full(8, 4096, np.int32), 32, 8, 128, 16,
                      ("bf16", "fp8", "turbo4"), "bf16", lognormal_sigma=0.5, chunk=512)
+    elif name == "prefill_hd256":
+        w = Workload("prefill_hd256", 8, np.full(8, 4096, np.int32), 32, 16, 256, 16,
+                     ("bf16", "turbo2", "turbo8"), "bf16", outlier_frac=0.0, chunk=512)
     else:
         raise KeyError(name)
     w.seed = seed

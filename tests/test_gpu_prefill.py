@@ -5,7 +5,8 @@ writes the cache; the same bytes are uploaded): max-abs <= 2e-3, mean-abs
 Every catalogue format; head_dim 64/128/256; GQA ratios 1, 2, 3, 4, 8;
 ragged chunks (a whole sequence, a single query, an empty chunk, a chunk
 longer than its sequence whose first queries attend nothing, chunks spanning
-several 64-row tiles); windows; block sizes 8/16/32; bf16 q and output."""
+several 64-row tiles); windows; block sizes 8/16/32; bf16 q and output;
+head_dim 256 (64-row tiles, 32-position steps) at GQA 1, 4 and 8."""
 import numpy as np
 import pytest
 import torch
@@ -72,6 +73,15 @@ def test_prefill_gqa_ratios(nq, nkv):
 @pytest.mark.parametrize("window", [1, 17, 100])
 def test_prefill_window(fmt, window):
     c = _prefill_case(fmt, LENS, CHUNKS, 8, 2, 128, seed=window)
+    assert_decode_close(_gpu(c, window=window), _oracle(c, window=window))
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "turbo2", "turbo8", "turbo4k_turbo3v", "fp8k_turbo2v"])
+@pytest.mark.parametrize("nq,nkv,window", [(2, 2, 0), (16, 2, 0), (8, 4, 33)])
+def test_prefill_hd256(fmt, nq, nkv, window):
+    """head_dim 256 runs 64-row tiles with 32-position steps: GQA 1 (64
+    queries per tile), GQA 8 (8 per tile), a window cutting steps."""
+    c = _prefill_case(fmt, [300, 77, 40], [200, 77, 9], nq, nkv, 256, seed=nq + window)
     assert_decode_close(_gpu(c, window=window), _oracle(c, window=window))
 
 
