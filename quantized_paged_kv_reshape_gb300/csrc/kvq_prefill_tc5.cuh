@@ -192,9 +192,9 @@ struct T5Cfg {
   // M of the accumulators (score rows per tile) and KV positions per step;
   // NSPLIT column parts per row (the four warps of a lane quadrant)
   static constexpr int NT = 512, ROWS = HD == 256 ? 64 : 128, TOK = HD == 256 ? 32 : 64, NSPLIT = 4;
-  // tokens per V dequantization item (head_dim 256: 2, so that 32-position
-  // steps still give every thread an item)
-  static constexpr int VTPI = HD == 256 ? 2 : 4;
+  // tokens per V dequantization item: 2, so that every thread has an item
+  // (4 per item measured 1-2% slower at head_dim 128 on GB300)
+  static constexpr int VTPI = 2;
   static constexpr int KPL = PfSide<KS>::PLANES, VPL = PfSide<VS>::PLANES;
   static constexpr int KROW = SideGeom<KS, HD>::ROW, KSROW = SideGeom<KS, HD>::SROW;
   static constexpr int VROW = SideGeom<VS, HD>::ROW, VSROW = SideGeom<VS, HD>::SROW;
@@ -316,12 +316,14 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
   const int st_end = p_last >= 0 ? p_last / TOK + 1 : st_begin;
 
   // ---- raw rows of step st (positions TOK st .. TOK st + TOK - 1) into buffer b
-  auto row_src = [&](int pos, int64_t& blk, int64_t& rr) -> bool {
-    if (pos < 0 || pos >= len) return false;
-    blk = a.block_tables[tab + (pos >> lbs)];
-    if (blk < 0 || (a.num_blocks > 0 && blk >= a.num_blocks)) return false;
-    rr = (int64_t)(pos & (a.bs - 1)) * a.nkv + kvh;
-    return true;
+  // Block id of this thread's row of step st (-1: no row there).  With the
+  // short steps of head_dim 256 it is loaded at the top of the step that
+  // issues the copies (its latency hidden behind the step: 1-3% faster);
+  // with 64-position steps that was 8% slower than loading it at the issue.
+  auto row_block = [&](int st) -> int64_t {
+    const int pos = st * TOK + tid / (NT / TOK);
+    if (st >= st_end || pos < 0 || pos >= len) return -1;
+    return a.block_tables[tab + (pos >> lbs)];
   };
   // Thread (row t = tid / PARTS, part = tid % PARTS) looks the row's block
   // up once and copies chunks part, part + PARTS, ... of its four rows:
@@ -336,13 +338,14 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
         cp_async<CHB>(dst + ch * CHB, (ok ? src : base) + ch * CHB, ok);
     }
   };
-  auto issue = [&](int st, int b) {
+  auto issue = [&](int st, int b, int64_t blk) {
     uint8_t* rb = raw + b * C::RAW;
     using KG = SideGeom<KS, HD>;
     using VG = SideGeom<VS, HD>;
     const int t = tid / PARTS, part = tid % PARTS;
-    int64_t blk = 0, rr = 0;
-    const bool ok = row_src(st * TOK + t, blk, rr);
+    const bool ok = blk >= 0 && (a.num_blocks <= 0 || blk < a.num_blocks);
+    const int64_t rr = (int64_t)((st * TOK + t) & (a.bs - 1)) * a.nkv + kvh;
+    if (!ok) blk = 0;
     const uint8_t* kb = a.k_cache + blk * a.k_bstride;
     const uint8_t* vb = a.v_cache + blk * a.v_bstride;
     copy_row(rb + t * KG::ROW, kb + rr * KG::ROW, a.k_cache, ok, part,
@@ -445,9 +448,9 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
   };
 
   // prologue: raw rows of the first two steps in flight, K of the first step
-  if (st_begin < st_end) issue(st_begin, 0);
+  if (st_begin < st_end) issue(st_begin, 0, row_block(st_begin));
   cp_async_commit();
-  if (st_begin + 1 < st_end) issue(st_begin + 1, 1);
+  if (st_begin + 1 < st_end) issue(st_begin + 1, 1, row_block(st_begin + 1));
   cp_async_commit();
   cp_async_wait<1>();
   __syncthreads();
@@ -458,6 +461,8 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     const int b = (st - st_begin) & 1;
     const uint32_t par = (uint32_t)((st - st_begin) & 1);
     __syncthreads();   // K of step st in its plane; raw rows of step st visible
+    int64_t blk2 = -1;
+    if constexpr (HD == 256) blk2 = row_block(st + 2);   // used by the copies issued at the end
     // ---- S = Q . K^T (q hi x K hi, q lo x K hi, q hi x K lo)
     if (tid == 0) {
       t5::fence_after();
@@ -589,7 +594,7 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
     // raw rows two steps ahead into this step's buffer (its K and V are in
     // their planes), issued after this step's last proxy fence: a proxy fence
     // also waits for the copies in flight (measured on GB300)
-    if (st + 2 < st_end) issue(st + 2, b);
+    if (st + 2 < st_end) issue(st + 2, b, HD == 256 ? blk2 : row_block(st + 2));
     cp_async_commit();
   }
   cp_async_wait<0>();
