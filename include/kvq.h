@@ -224,7 +224,9 @@ size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *   sparse_v_threshold  0 = exact; > 0 drops the V term of a position whose
  *                weight (normalised by the part of the sequence one warp has
  *                seen so far, which over-estimates the global weight, so it
- *                never drops more) is <= threshold
+ *                never drops more) is <= threshold; a 16-position slab whose
+ *                weights are all dropped skips its V dequantization and P.V
+ *                products.  The denominator keeps every weight.
  *   workspace    device, >= kvq_decode_workspace_bytes(...) bytes, 16-byte
  *                aligned, all zero on entry.  Every call leaves the whole
  *                workspace zero again, so one zeroed once can be reused by
@@ -271,7 +273,8 @@ kvq_status kvq_paged_decode(
  *   out          device, out_dtype, contiguous [cu_q[num_seqs], num_q_heads, head_dim]
  *   other arguments as kvq_paged_decode (no workspace; no sparse-V skip).
  * One kernel launch: a CTA per (tile of query rows, kv head, sequence); the
- * contraction runs on tensor cores. */
+ * products run on the tcgen05 tensor cores with accumulators in tensor
+ * memory (128-row tiles for head_dim 64/128, 64-row tiles for 256). */
 kvq_status kvq_paged_prefill(
     const void* q, kvq_dtype q_dtype, int64_t q_stride,
     const int32_t* cu_q, int32_t max_chunk,
