@@ -850,6 +850,23 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
       p0 = tok0 >> lbs;
       const int p1 = ((tok_end - 1) >> lbs) + 1;
       tab = (int64_t)sq * a.max_blocks;
+      // Block ids of the stretch's pages (-1 = outside the pool).
+      for (int i = tid; i < p1 - p0; i += NT) {
+        const int64_t b = a.block_tables[tab + p0 + i];
+        const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
+        if (bad && a.err) atomicOr(a.err, 2);
+        blk_s[i] = bad ? -1 : (int)b;
+      }
+      __syncthreads();
+      if (tid == 0) st[5] = sa + nsl;
+      const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
+#pragma unroll
+      for (int s = 0; s < C::NST - 1; ++s) {
+        if (s < my) issue(s);
+        cp_async_commit();
+      }
+      // The unit's queries are staged after its first copies are in flight
+      // (those need only the block ids), so their loads overlap the copies.
       if (first_stretch) {
         // ---- queries (rotated when K is stored rotated), rows >= rep are zero
         for (int j = warp; j < 8; j += NW) {
@@ -868,21 +885,7 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
 #pragma unroll
           for (int i = 0; i < E; ++i) q_s[j * HD + lane * E + i] = xq[i];
         }
-      }
-      // Block ids of the stretch's pages (-1 = outside the pool).
-      for (int i = tid; i < p1 - p0; i += NT) {
-        const int64_t b = a.block_tables[tab + p0 + i];
-        const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
-        if (bad && a.err) atomicOr(a.err, 2);
-        blk_s[i] = bad ? -1 : (int)b;
-      }
-      __syncthreads();
-      if (tid == 0) st[5] = sa + nsl;
-      const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
-#pragma unroll
-      for (int s = 0; s < C::NST - 1; ++s) {
-        if (s < my) issue(s);
-        cp_async_commit();
+        __syncthreads();   // q_s visible
       }
       if (first_stretch) {
 #pragma unroll
