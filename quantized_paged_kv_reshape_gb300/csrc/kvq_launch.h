@@ -60,7 +60,7 @@ struct DecodeArgs {  // arguments of the paged decode (decode_tc_kernel)
 };
 
 
-struct PrefillArgs {  // arguments of the chunked prefill (prefill_tc_kernel)
+struct PrefillArgs {  // arguments of the chunked prefill (prefill_tc5_kernel)
   const void* q;
   int64_t q_stride;          // elements between query tokens
   int q_bf16;
