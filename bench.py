@@ -64,6 +64,10 @@ TRAFFIC = {
     ("llama8b", "fp8"): 270_267_136,
     ("llama8b", "turbo4"): 152_794_624,
 }
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# prefill launch (the slowest format of the workload), from the 1-pass ncu
+# capture summarised in profiles/ (None when the kernel changed after it).
+PF_TRAFFIC = {}
 # smsp__inst_executed.sum per launch (warp-instructions) of the same capture:
 # the second roofline of the decode formats that are issue bound.  Issue
 # peak = 4 warp-instructions per cycle per SM (one per sub-partition) x the
@@ -709,7 +713,8 @@ def run_prefill(args):
             "per_layer": per_layer,
             "roofline": {"kernel": f"prefill_tc5_kernel ({dom})", "bound": "tensor",
                          "achieved": per_layer[dom]["tflops"], "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(per_layer[dom]["tflops"] / peak, 4), "traffic": None,
+                         "frac": round(per_layer[dom]["tflops"] / peak, 4),
+                         "traffic": PF_TRAFFIC.get((args.workload, dom)),
                          "peak_kind": "measured bf16 dense, burst" if pk else "fallback",
                          "flops_per_layer": flops},
             "gpu_launches": 2 * len(fmts) * args.steps, "clocks": clocks}))

@@ -150,14 +150,16 @@ def test_gemma_write_and_decode_full(fmt):
     _check(w, fmt, sampled=[5])
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp8", "turbo4"])
-def test_prefill_full(fmt):
-    """The chunked-prefill workload at full size (8 x 4096 positions, the last
-    512 of every sequence the chunk, the launch bench.py times): queries of
-    two sampled sequences against the oracle, the first 8 and the last 8 of
-    each chunk (the first ones through the oracle's causal reading of a
-    shorter sequence)."""
-    w = W.make("prefill")
+@pytest.mark.parametrize("name,fmt", [("prefill", "bf16"), ("prefill", "fp8"), ("prefill", "turbo4"),
+                                      ("prefill_hd256", "bf16"), ("prefill_hd256", "turbo2"),
+                                      ("prefill_hd256", "turbo8")])
+def test_prefill_full(name, fmt):
+    """The chunked-prefill workloads at full size (8 x 4096 positions, the
+    last 512 of every sequence the chunk, the launches bench.py times; head_dim
+    128 and the Gemma-shaped head_dim 256): queries of two sampled sequences
+    against the oracle, the first 8 and the last 8 of each chunk (the first
+    ones through the oracle's causal reading of a shorter sequence)."""
+    w = W.make(name)
     nq, nkv, hd, bs, C = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.chunk
     sampled = [0, 5]
     st = _fill(w, fmt, sampled)
