@@ -67,7 +67,14 @@ TRAFFIC = {
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # prefill launch (the slowest format of the workload), from the 1-pass ncu
 # capture summarised in profiles/ (None when the kernel changed after it).
-PF_TRAFFIC = {}
+PF_TRAFFIC = {
+    ("prefill", "bf16"): 190_333_952,
+    ("prefill", "fp8"): 113_056_000,
+    ("prefill", "turbo4"): 78_117_120,
+    ("prefill_hd256", "bf16"): 667_113_984,
+    ("prefill_hd256", "turbo2"): 190_637_568,
+    ("prefill_hd256", "turbo8"): 423_295_232,
+}
 # smsp__inst_executed.sum per launch (warp-instructions) of the same capture:
 # the second roofline of the decode formats that are issue bound.  Issue
 # peak = 4 warp-instructions per cycle per SM (one per sub-partition) x the
