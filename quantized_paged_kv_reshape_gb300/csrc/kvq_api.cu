@@ -314,7 +314,10 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
   const Codebooks& cb = codebooks();
   const bool bf = in_dtype == KVQ_DTYPE_BF16;
   const int el = bf ? 2 : 4;
-  const int va = bf ? (hd / 32) * 2 : 8;  // bytes of one lane's vector load
+  // bytes of one lane's vector load: a row takes 16 lanes (head_dim 64/128)
+  // or 32 (256), head_dim / lanes elements each
+  const int lanes = hd == 256 ? 32 : 16;
+  const int va = bf ? (hd / lanes) * 2 : 8;
   const bool vec = ((uintptr_t)key % va == 0) && ((uintptr_t)value % va == 0) &&
                    (key_stride * el) % va == 0 && (value_stride * el) % va == 0;
   WriteArgs a{};
@@ -340,9 +343,10 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
   a.k_side = ks;
   a.v_side = vs;
   a.err = error_flag;
-  const int64_t rows = (int64_t)num_tokens * nkv * 2;
+  // units = (token pair or token, side, kv head): 32 / lanes rows each
+  const int64_t units = ((int64_t)num_tokens + 32 / lanes - 1) / (32 / lanes) * nkv * 2;
   const int sms = sm_count();
-  const int64_t want = (rows + 15) / 16;   // 8 warps x 2 rows per CTA iteration
+  const int64_t want = (units + 15) / 16;   // 8 warps x 2 units per CTA iteration
   const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 32;
   const int grid = (int)(want < cap ? want : cap);
   cudaError_t e = launch_cache_write(a, cb, hd, bf, vec, grid, (cudaStream_t)stream);

@@ -102,14 +102,15 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
 
 // --------------------------------------------------------- rotation
 
-// Normalised Walsh-Hadamard transform of a head_dim row held by one warp,
-// E = head_dim / 32 consecutive elements per lane (element lane*E + i).
-// Butterfly stages h = 1, 2, 4, ... in that order; each stage maps the pair
-// (x[j], x[j+h]) (bit h of j clear) to (x[j] + x[j+h], x[j] - x[j+h]).
-// Stages h < E stay in registers, the others pair lane with lane ^ (h/E).
-// Finally every element is multiplied once by inv_sqrt_n.  The arithmetic
-// per element is identical whatever lane layout runs it.
-template <int E>
+// Normalised Walsh-Hadamard transform of a head_dim row held by LANES
+// consecutive lanes of a warp (32, or 16 for a row per half-warp), E =
+// head_dim / LANES consecutive elements per lane (element (lane % LANES)*E
+// + i).  Butterfly stages h = 1, 2, 4, ... in that order; each stage maps
+// the pair (x[j], x[j+h]) (bit h of j clear) to (x[j] + x[j+h], x[j] -
+// x[j+h]).  Stages h < E stay in registers, the others pair lane with lane ^
+// (h/E).  Finally every element is multiplied once by inv_sqrt_n.  The
+// arithmetic per element is identical whatever lane layout runs it.
+template <int E, int LANES = 32>
 __device__ __forceinline__ void fwht_warp(float (&x)[E], int lane, float inv_sqrt_n) {
 #pragma unroll
   for (int h = 1; h < E; h <<= 1) {
@@ -123,7 +124,7 @@ __device__ __forceinline__ void fwht_warp(float (&x)[E], int lane, float inv_sqr
     }
   }
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
+  for (int m = 1; m < LANES; m <<= 1) {
     // lower lane holds a = x[j], partner b: a + b; upper lane holds b,
     // partner a: a - b = fma(b, -1, a) (the same single rounding)
     const float sg = (lane & m) ? -1.f : 1.f;
