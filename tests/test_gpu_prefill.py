@@ -114,3 +114,34 @@ def test_prefill_chunk_of_one_is_decode():
     torch.cuda.synchronize()
     got = _gpu(c)
     assert np.abs(got - dec.cpu().numpy()).max() <= 2e-3
+
+
+def test_prefill_graph_replay():
+    """The prefill captures into a CUDA graph: after the query buffer is
+    refilled, each replay matches the oracle for the new queries."""
+    c = _prefill_case("turbo4", [300, 77], [64, 20], 8, 2, 128, seed=41)
+    dev = "cuda"
+    kpool = torch.from_numpy(c["kc"].reshape(c["num_blocks"], c["kst"])).to(dev)
+    vpool = torch.from_numpy(c["vc"].reshape(c["num_blocks"], c["vst"])).to(dev)
+    q = torch.from_numpy(c["qp"]).to(dev)
+    cu = torch.from_numpy(c["cu"]).to(dev)
+    tables = torch.from_numpy(c["tables"]).to(dev)
+    lens = torch.from_numpy(c["lens"]).to(dev)
+    out = torch.empty_like(q)
+
+    def call():
+        ops.paged_prefill(q, cu, max(c["chunks"]), kpool, vpool, tables, lens, c["fmt"], c["nkv"],
+                          c["bs"], out=out, k_scale=c["k_scale"], v_scale=c["v_scale"])
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(43)
+    for qn in (rng.standard_normal(c["qp"].shape).astype(np.float32), c["qp"]):
+        q.copy_(torch.from_numpy(qn))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_decode_close(out.cpu().numpy().astype(np.float64), _oracle(c, q=qn))

@@ -143,3 +143,49 @@ def test_write_near_decision_boundaries(fmt, hd):
     torch.cuda.synchronize()
     got = kpool.cpu().numpy().reshape(-1)
     assert np.array_equal(got, kc), f"{int((got != kc).sum())} bytes differ"
+
+
+def test_write_graph_replay():
+    """The write captures into a CUDA graph, as a serving step replays it:
+    after the input rows and the slots are refilled, each replay stores the
+    oracle's bytes for the new rows (an odd token count: the last warp's
+    second half-warp row has no token)."""
+    fmt, hd, nkv, bs, nb, ntok = "turbo4k_turbo3v", 128, 2, 16, 7, 31
+    kside, vside = oracle.kv_pair(fmt)
+    kst = (oracle.block_bytes(kside, bs, nkv, hd) + 15) // 16 * 16
+    vst = (oracle.block_bytes(vside, bs, nkv, hd) + 15) // 16 * 16
+    dev = "cuda"
+    k_d = torch.zeros((ntok, nkv * hd), device=dev)
+    v_d = torch.zeros((ntok, nkv * hd), device=dev)
+    s_d = torch.full((ntok,), -1, dtype=torch.int64, device=dev)
+    kpool = torch.zeros((nb, kst), dtype=torch.uint8, device=dev)
+    vpool = torch.zeros((nb, vst), dtype=torch.uint8, device=dev)
+
+    def call():
+        ops.cache_write(k_d, v_d, kpool, vpool, s_d, fmt, nkv, hd, bs)
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(17)
+    for _ in range(2):
+        k = rng.standard_normal((ntok, nkv, hd)).astype(np.float32)
+        v = rng.standard_normal((ntok, nkv, hd)).astype(np.float32)
+        slots = rng.permutation(nb * bs)[:ntok].astype(np.int64)
+        slots[rng.choice(ntok, 3, replace=False)] = -1
+        k_d.copy_(torch.from_numpy(k.reshape(ntok, -1)))
+        v_d.copy_(torch.from_numpy(v.reshape(ntok, -1)))
+        s_d.copy_(torch.from_numpy(slots))
+        kpool.zero_()
+        vpool.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        kc = np.zeros(nb * kst, np.uint8)
+        vc = np.zeros(nb * vst, np.uint8)
+        oracle.cache_write(kside, k, kc, slots, nkv, hd, bs, kst)
+        oracle.cache_write(vside, v, vc, slots, nkv, hd, bs, vst)
+        assert np.array_equal(kpool.cpu().numpy().reshape(-1), kc)
+        assert np.array_equal(vpool.cpu().numpy().reshape(-1), vc)
