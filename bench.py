@@ -60,9 +60,9 @@ WORKLOAD_DESC = {
 # decode launch, from the ncu capture summarised in profiles/ (None when the
 # kernel changed after the capture).
 TRAFFIC = {
-    ("llama8b", "bf16"): 541_566_720,
-    ("llama8b", "fp8"): 270_267_136,
-    ("llama8b", "turbo4"): 152_794_624,
+    ("llama8b", "bf16"): 541_548_288,
+    ("llama8b", "fp8"): 270_268_416,
+    ("llama8b", "turbo4"): 152_777_216,
 }
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # prefill launch (the slowest format of the workload), from the 1-pass ncu
@@ -80,9 +80,9 @@ PF_TRAFFIC = {
 # peak = 4 warp-instructions per cycle per SM (one per sub-partition) x the
 # SMs x the SM clock sampled during the timed region.
 WARP_INSTR = {
-    ("llama8b", "bf16"): 25_479_173,
-    ("llama8b", "fp8"): 29_086_821,
-    ("llama8b", "turbo4"): 65_006_533,
+    ("llama8b", "bf16"): 25_501_653,
+    ("llama8b", "fp8"): 29_071_653,
+    ("llama8b", "turbo4"): 64_988_213,
 }
 
 
