@@ -55,9 +55,10 @@ def _prefill(c, window=0, kc=None):
                                 window=window)
 
 
+@pytest.mark.parametrize("hd", [64, 256])
 @pytest.mark.parametrize("fmt", ["bf16", "fp8", "turbo4", "turbo4k_turbo3v", "nvfp4", "turbo8"])
-def test_chunk_of_one_is_decode(fmt):
-    c = _case(fmt, [37, 50, 16], [1, 1, 1])
+def test_chunk_of_one_is_decode(fmt, hd):
+    c = _case(fmt, [37, 50, 16], [1, 1, 1], hd=hd)
     got = _prefill(c)
     ref = oracle.paged_decode(c["q"], c["kc"], c["vc"], c["tables"], c["lens"], c["nkv"], c["hd"],
                               c["bs"], c["kst"], c["vst"], fmt, k_scale=c["ks"], v_scale=c["vs"])
