@@ -175,12 +175,6 @@ def algorithmic_decode_bytes(fmt, seq_lens, nkv, hd, bs, window=0):
     return int(att.sum()) * per_tok
 
 
-def decode_kernel_name(fmt):
-    """Name of the decode kernel libkvq launches for this format (label only):
-    every catalogue format runs on the tensor-core kernel."""
-    return "decode_tc_kernel"
-
-
 def write_bytes(fmt, ntok, nkv, hd, bs, in_bytes=2):
     from quantized_paged_kv_reshape_gb300 import ops
     out = sum(ops.block_bytes(fmt, side, bs, nkv, hd) // bs for side in (0, 1)) * ntok
