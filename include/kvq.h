@@ -308,11 +308,19 @@ kvq_status kvq_paged_prefill(
  * it zero).  Nothing is allocated (no cudaMalloc / cudaFree).
  *   - Returns KVQ_ERR_WORKSPACE if kvq_decode_workspace_bytes(...) for these
  *     arguments exceeds KVQ_NOALLOC_SCRATCH_BYTES.
- *   - The first call with a given device current looks the array's device
- *     address up (cudaGetSymbolAddress) and caches it; make that first call
- *     before any stream capture.
+ *   - The array's device address is looked up (cudaGetSymbolAddress) on
+ *     every call, so a new context on the device (after cudaDeviceReset, or
+ *     once the primary context was released and created again) is followed.
+ *     A call made while its stream is being captured reuses the address that
+ *     the last uncaptured call on the same device looked up, and returns
+ *     KVQ_ERR_CUDA if there was none: make the first call on a device before
+ *     any stream capture.
  *   - Every call shares the one array: calls whose kernels overlap on the GPU
- *     (different streams, or different host threads) race.  Serialize them. */
+ *     (different streams, or different host threads) race.  Serialize them.
+ *   - A call that returns KVQ_ERR_CUDA after its launch was attempted has
+ *     queued, on its stream, a clear of the part of the array it may have
+ *     touched.  If the context itself has failed, the array is undefined
+ *     until the context is created again, which loads a fresh, zero copy. */
 kvq_status kvq_paged_decode_noalloc(
     const void* q, kvq_dtype q_dtype, int64_t q_stride,
     const void* k_cache, const void* v_cache,

@@ -39,7 +39,7 @@ Inputs are read through per-token element strides ``key_stride`` /
 launcher passes both strides, so K/V may be views of a fused QKV buffer).
 
 Pins: tests/test_oracle_write.py (hand-worked 16-element groups in
-tests/golden/turbo4_groups.txt, brute-force packing round trips, an
+tests/golden/turbo_groups.txt, brute-force packing round trips, an
 independent big-integer packing of 3-bit codes, the unit-scale MSE against
 the closed-form distortion, and the byte arithmetic of the section sizes).
 """

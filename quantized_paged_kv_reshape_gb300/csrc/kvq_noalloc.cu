@@ -1,21 +1,29 @@
 // Paged decode for callers that cannot allocate device memory.
 //
 // kvq_paged_decode needs a caller-provided scratch buffer for the partial
-// results of rows that several CTAs share and their merge counters.  Some callers cannot get one: a runtime that has already
-// handed all device memory to its own pool, a plugin host that forbids
-// device allocations by its plugins, or a latency-critical loop where
-// cudaMalloc (which may synchronize the device) is not acceptable.  This
-// entry point runs the same kernels with the scratch taken from a fixed
-// array compiled into the library instead; it allocates nothing.
+// results of rows that several CTAs share and their merge counters.  Some
+// callers cannot get one: a runtime that has already handed all device memory
+// to its own pool, a plugin host that forbids device allocations by its
+// plugins, or a latency-critical loop where cudaMalloc (which may synchronize
+// the device) is not acceptable.  This entry point runs the same kernels with
+// the scratch taken from a fixed array compiled into the library instead; it
+// allocates nothing.
 //
 // The array lives in every GPU that loads the library, for the life of the
 // process.  Host code must not use the array's name as a device address (on
-// the host it only names a stand-in); the device address is looked up with
-// cudaGetSymbolAddress once per device, on the first call made with that
-// device current, and cached.  Make that first call before any stream
-// capture.  All calls share the one array, so calls whose kernels overlap on
-// the GPU race.  The array is zero when the library loads (static storage)
-// and every decode leaves it zero, which is the state the next call needs.
+// the host it only names a stand-in).  The device address belongs to the copy
+// of the library's device code loaded into the current context, and a new
+// context (after cudaDeviceReset, or once the primary context was released
+// and created again) loads a new copy, so the address is looked up with
+// cudaGetSymbolAddress on every call.  The one exception is a call made
+// while its stream is being captured into a graph: it reuses the address that
+// the last uncaptured call on the same device looked up (a lookup could load
+// the module, which a capture does not allow), and fails if there was none.
+// All calls share the one array, so calls whose kernels overlap on the GPU
+// race.  The array is zero when its copy is loaded (static storage) and every
+// decode leaves it zero, which is the state the next call needs; a call that
+// fails after the launch was attempted queues a clear of the part it may have
+// touched before it returns.
 #include "../../include/kvq.h"
 
 #include <cuda_runtime.h>
@@ -33,26 +41,38 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+void* g_last_lookup[kMaxDevices] = {};   // per device: the last uncaptured call's address
 
-kvq_status scratch_for_current_device(void** out) {
+kvq_status scratch_address(cudaStream_t stream, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     kvq::record_error("no usable current CUDA device for the built-in decode scratch");
     return KVQ_ERR_CUDA;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) {
+    kvq::record_error("cudaStreamIsCapturing failed on the decode stream");
+    return KVQ_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess || !p) {
+      g_last_lookup[dev] = nullptr;
       kvq::record_error("cudaGetSymbolAddress of the built-in decode scratch failed");
       return KVQ_ERR_CUDA;
     }
-    g_scratch_ptr[dev] = p;
+    g_last_lookup[dev] = p;
+  } else if (!g_last_lookup[dev]) {
+    kvq::record_error(
+        "the first decode without a workspace on this device was made during stream capture; "
+        "make one uncaptured call first");
+    return KVQ_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_last_lookup[dev];
   return KVQ_OK;
 }
 
@@ -76,11 +96,18 @@ extern "C" kvq_status kvq_paged_decode_noalloc(
     return KVQ_ERR_WORKSPACE;
   }
   void* scratch = nullptr;
-  const kvq_status st = scratch_for_current_device(&scratch);
+  const kvq_status st = scratch_address((cudaStream_t)stream, &scratch);
   if (st != KVQ_OK) return st;
-  return kvq_paged_decode(q, q_dtype, q_stride, k_cache, v_cache, out, out_dtype, block_tables,
-                          max_blocks_per_seq, seq_lens, num_seqs, num_blocks, num_q_heads,
-                          num_kv_heads, head_dim, block_size, k_block_stride_bytes,
-                          v_block_stride_bytes, sm_scale, k_scale, v_scale, sliding_window,
-                          sparse_v_threshold, scratch, kScratchBytes, fmt, error_flag, stream);
+  const kvq_status r = kvq_paged_decode(
+      q, q_dtype, q_stride, k_cache, v_cache, out, out_dtype, block_tables, max_blocks_per_seq,
+      seq_lens, num_seqs, num_blocks, num_q_heads, num_kv_heads, head_dim, block_size,
+      k_block_stride_bytes, v_block_stride_bytes, sm_scale, k_scale, v_scale, sliding_window,
+      sparse_v_threshold, scratch, kScratchBytes, fmt, error_flag, stream);
+  if (r == KVQ_ERR_CUDA && need > 0) {
+    // The launch was attempted: return the part of the array this call may
+    // have touched to zero (stream-ordered; kvq_last_error keeps the launch's
+    // message).
+    cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream);
+  }
+  return r;
 }

@@ -16,10 +16,13 @@ pytestmark = pytest.mark.gpu
 
 
 def run_write(fmt, hd, in_dtype, nkv=2, bs=16, num_blocks=7, ntok=45, seed=0, pad=32,
-              bad_slot=False):
+              bad_slot=False, row_extra=8, shift=0):
+    """Fused QKV rows of (nq + 2 nkv) * hd + row_extra elements; K and V start
+    `shift` elements after their heads' natural offsets in the row."""
+    assert 0 <= shift <= row_extra
     rng = np.random.default_rng(seed)
     nq = 2 * nkv
-    row = (nq + 2 * nkv) * hd + 8           # fused QKV row, stride != nkv*hd
+    row = (nq + 2 * nkv) * hd + row_extra   # fused QKV row, stride != nkv*hd
     fused = rng.standard_normal((ntok, row)).astype(np.float32)
     fused[:, rng.choice(row, 6, replace=False)] *= 10.0      # outlier channels
     fused[3, :] = 0.0                                         # an all-zero token
@@ -29,7 +32,7 @@ def run_write(fmt, hd, in_dtype, nkv=2, bs=16, num_blocks=7, ntok=45, seed=0, pa
     slots[rng.choice(ntok, 5, replace=False)] = -1
     if bad_slot:
         slots[7] = num_blocks * bs + 3
-    koff, voff = nq * hd, (nq + nkv) * hd
+    koff, voff = nq * hd + shift, (nq + nkv) * hd + shift
     kview = fused[:, koff:koff + nkv * hd].reshape(ntok, nkv, hd)
     vview = fused[:, voff:voff + nkv * hd].reshape(ntok, nkv, hd)
     kside, vside = oracle.kv_pair(fmt)
@@ -60,6 +63,21 @@ def run_write(fmt, hd, in_dtype, nkv=2, bs=16, num_blocks=7, ntok=45, seed=0, pa
 @pytest.mark.parametrize("fmt", ALL_FORMATS)
 def test_write_bit_exact(fmt, hd, in_dtype):
     kc, vc, kg, vg, err = run_write(fmt, hd, in_dtype, seed=hd)
+    assert err == 0
+    assert np.array_equal(kc, kg), f"K bytes differ at {np.flatnonzero(kc != kg)[:8]}"
+    assert np.array_equal(vc, vg), f"V bytes differ at {np.flatnonzero(vc != vg)[:8]}"
+
+
+@pytest.mark.parametrize("row_extra,shift", [(1, 0), (3, 1)])
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hd", [64, 128, 256])
+@pytest.mark.parametrize("fmt", ALL_FORMATS)
+def test_write_unaligned_strides(fmt, hd, in_dtype, row_extra, shift):
+    """Key/value rows whose per-token stride (an odd element count) or start
+    (one element past a 16-byte boundary) breaks the lanes' vector alignment:
+    the library must take the per-element loads and store the same bytes."""
+    kc, vc, kg, vg, err = run_write(fmt, hd, in_dtype, seed=hd + 7, row_extra=row_extra,
+                                    shift=shift)
     assert err == 0
     assert np.array_equal(kc, kg), f"K bytes differ at {np.flatnonzero(kc != kg)[:8]}"
     assert np.array_equal(vc, vg), f"V bytes differ at {np.flatnonzero(vc != vg)[:8]}"
