@@ -159,6 +159,26 @@ def slowest_rank(values, dev):
     return [float(v) for v in t]
 
 
+def parallelism(world):
+    if world == 1:
+        return "one GPU"
+    return (f"dp{world}: a {world}x batch, sequence i on rank i mod {world} "
+            "(no collective on the data path; NCCL only for the barrier and the slowest rank's time)")
+
+
+def relaunch_under_torchrun(n):
+    """`--gpus N` outside torchrun: run this same command as N ranks, one per
+    GPU, through torch.distributed.run on this node."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def job_rate(bytes_per_rank_step, world_size, ms_per_step):
     """Whole-job throughput in GB/s: every rank processes its own units (weak
     scaling), the step lasts as long as the slowest rank."""
@@ -250,9 +270,9 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
     _abi.lib()
 
-    w = W.make(args.workload, seed=rank)
+    w = W.rank_workload(args.workload, ws, rank)
     if args.num_seqs and args.num_seqs != w.num_seqs:
-        w = W.make(args.workload, seed=rank, num_seqs=args.num_seqs,
+        w = W.make(args.workload, num_seqs=args.num_seqs,
                    seq_lens=np.resize(w.seq_lens, args.num_seqs).astype(np.int32))
     nkv, nq, hd, bs = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size
     nseq = w.num_seqs
@@ -522,7 +542,7 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD_DESC[args.workload].format(nseq=nseq),
                    "formats": fmts, "windows": windows,
                    "l2": f"inputs larger than L2 ({sum(dec_bytes.values()) / 1e6:.0f} MB of cache per step)",
-                   "parallelism": f"replicas x{ws} (sequences sharded, no collective)",
+                   "parallelism": parallelism(ws),
                    "launch": launch_mode},
         "per_layer": per_layer,
         "cache_write": per_write,
@@ -657,7 +677,7 @@ def run_prefill(args):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     _abi.lib()
-    w = W.make(args.workload, seed=rank)
+    w = W.rank_workload(args.workload, ws, rank)
     nkv, nq, hd, bs, C = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size, w.chunk
     nseq = w.num_seqs
     lens_np = np.asarray(w.seq_lens, np.int64)
@@ -749,7 +769,7 @@ def run_prefill(args):
             "data": "synthetic",
             "config": {"workload": WORKLOAD_DESC[args.workload].format(nseq=nseq), "formats": fmts,
                        "l2": "caches far above L2 between steps",
-                       "parallelism": f"replicas x{ws} (sequences sharded, no collective)"},
+                       "parallelism": parallelism(ws)},
             "per_layer": per_layer,
             "roofline": {"kernel": f"prefill_tc5_kernel ({dom})", "bound": "tensor",
                          "achieved": per_layer[dom]["tflops"], "peak": peak, "unit": "TFLOP/s",
@@ -800,6 +820,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch_under_torchrun(args.gpus))
     if args.impl == "reference":
         run_reference(args)
     elif args.workload.startswith("prefill"):

@@ -35,5 +35,5 @@ from .cache_write import (  # noqa: F401
     quantize_rows, quantize_rotated, quantize_nvfp4, pack_codes, unpack_codes, encode_rows_bytes,
     cache_write,
 )
-from .decode import dequantize_rows, gather_side, paged_decode  # noqa: F401
+from .decode import attend, dequantize_rows, gather_side, paged_decode  # noqa: F401
 from .prefill import paged_prefill  # noqa: F401

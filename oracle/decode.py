@@ -30,7 +30,9 @@ The plain definition, in fp64:
 
 Pins: tests/test_oracle_decode.py (an independent naive attention loop on
 BF16-exact K/V, seq_len 1 -> v_0, q = 0 -> mean of V, window 1 -> last V,
-and the rotated-basis identity checked against this plain definition).
+and the rotated-basis identity checked against this plain definition;
+``attend`` on given K/V equals the paged decode of a BF16 cache holding the
+same bf16-exact rows, and the naive loop directly).
 """
 
 import math
@@ -99,6 +101,38 @@ def attended_positions(seq_len, window):
     return np.arange(lo, seq_len, dtype=np.int64)
 
 
+def attend(q, k, v, sm_scale=None, sparse_v_threshold=0.0):
+    """fp64 output [nq, hd] of one query per head over given K/V rows.
+
+    "combs_models/kv.rs", ``attend`` for one query (no mask) with
+    ``repeat_kv``: q [nq, hd], k and v [n, nkv, hd] (the attended positions,
+    in the original basis); query head j reads kv head j // (nq / nkv).
+    scores = (q . k) * sm_scale, P = softmax over the n positions, out = P.V;
+    sparse-V drops terms whose normalised weight is <= the threshold (the
+    denominator kept).  n = 0 gives zeros.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    nq, hd = q.shape
+    nkv = k.shape[1]
+    rep = nq // nkv
+    if sm_scale is None or sm_scale == 0:
+        sm_scale = 1.0 / math.sqrt(hd)
+    out = np.zeros((nq, hd), dtype=np.float64)
+    if k.shape[0] == 0:
+        return out
+    for j in range(nq):
+        kh = j // rep
+        scores = (k[:, kh, :] @ q[j]) * sm_scale
+        w = np.exp(scores - scores.max())
+        p = w / w.sum()
+        if sparse_v_threshold > 0:
+            p = np.where(p <= sparse_v_threshold, 0.0, p)
+        out[j] = p @ v[:, kh, :]
+    return out
+
+
 def paged_decode(q, k_cache, v_cache, block_tables, seq_lens, nkv, hd,
                  block_size, k_block_stride, v_block_stride, fmt,
                  sm_scale=None, k_scale=None, v_scale=None, window=0,
@@ -106,10 +140,7 @@ def paged_decode(q, k_cache, v_cache, block_tables, seq_lens, nkv, hd,
     """fp64 output [num_seqs, nq, hd] of one-query-per-sequence attention."""
     q = np.asarray(q, dtype=np.float64)
     nseq, nq, _ = q.shape
-    rep = nq // nkv
     k_side, v_side = F.kv_pair(fmt)
-    if sm_scale is None or sm_scale == 0:
-        sm_scale = 1.0 / math.sqrt(hd)
     block_tables = np.asarray(block_tables, dtype=np.int64)
     out = np.zeros((nseq, nq, hd), dtype=np.float64)
     for s in range(nseq):
@@ -122,12 +153,5 @@ def paged_decode(q, k_cache, v_cache, block_tables, seq_lens, nkv, hd,
                         k_block_stride, k_scale)
         v = gather_side(v_cache, v_side, blocks, offs, nkv, hd, block_size,
                         v_block_stride, v_scale)
-        for j in range(nq):
-            kh = j // rep
-            scores = (k[:, kh, :] @ q[s, j]) * sm_scale
-            w = np.exp(scores - scores.max())
-            p = w / w.sum()
-            if sparse_v_threshold > 0:
-                p = np.where(p <= sparse_v_threshold, 0.0, p)
-            out[s, j] = p @ v[:, kh, :]
+        out[s] = attend(q[s], k, v, sm_scale, sparse_v_threshold)
     return out

@@ -197,3 +197,45 @@ def fused_qkv(num_tokens, row_elems, nq, nkv, hd, seed=0):
     rng = np.random.default_rng([seed, 9])
     assert row_elems >= (nq + 2 * nkv) * hd
     return rng.standard_normal((num_tokens, row_elems), dtype=np.float32)
+
+
+# ------------------------------------------------------------ sharding over ranks
+#
+# Weak scaling over `world` GPUs: the job decodes a batch `world` times the
+# workload's, and the sequences, which share nothing, are dealt out round
+# robin (rank r owns global sequences r, r + world, ...).  Each rank holds the
+# pages of its own sequences; no data crosses ranks.
+
+def global_lengths(name, world=1, seed=0):
+    """int32 lengths of the `world`-times batch of workload `name` (world 1:
+    the workload's own batch)."""
+    base = make(name, seed=seed)
+    if world == 1:
+        return base.seq_lens.copy()
+    if name == "ragged":
+        rng = np.random.default_rng([seed, world])
+        return rng.integers(512, 16384, size=base.num_seqs * world,
+                            endpoint=True).astype(np.int32)
+    return np.tile(base.seq_lens, world).astype(np.int32)
+
+
+def shard_sequences(num_seqs, world, rank):
+    """Global indices of the sequences rank `rank` of `world` owns."""
+    if not 0 <= rank < world:
+        raise ValueError(f"rank {rank} outside a world of {world}")
+    return np.arange(rank, num_seqs, world, dtype=np.int64)
+
+
+def rank_workload(name, world=1, rank=0, seed=0):
+    """The sub-workload of rank `rank`: its sequences of the `world`-times
+    batch, with their lengths; ``notes['global_seqs']`` lists their global
+    indices.  For world 1 this is the workload itself."""
+    lens = global_lengths(name, world, seed)
+    idx = shard_sequences(lens.size, world, rank)
+    if world == 1:
+        w = make(name, seed=seed)
+    else:
+        w = make(name, seed=seed, num_seqs=int(idx.size), seq_lens=lens[idx])
+    w.notes["global_seqs"] = idx
+    w.notes["world"] = world
+    return w

@@ -135,3 +135,33 @@ def test_sparse_v_drops_small_weights_only():
     huge = paged_decode(**a, sparse_v_threshold=1.0)
     assert np.max(np.abs(dense - sparse)) < 0.05
     assert not huge.any()
+
+
+def test_attend_on_given_rows():
+    """attend() on K/V rows equals the naive loop, and the paged decode of a
+    BF16 cache that holds the same (bf16-exact) rows, window included."""
+    from oracle.decode import attend
+    from oracle.numformats import bf16_decode, bf16_encode
+    rng = np.random.default_rng(5)
+    n, nq, nkv, hd, bs = 37, 6, 3, 64, 16
+    k = bf16_decode(bf16_encode(rng.standard_normal((n, nkv, hd)).astype(np.float32)))
+    v = bf16_decode(bf16_encode(rng.standard_normal((n, nkv, hd)).astype(np.float32)))
+    q = rng.standard_normal((nq, hd))
+    got = attend(q, k, v)
+    for j in range(nq):
+        ref = naive(q[j], k[:, j // 2], v[:, j // 2], 1 / 8)
+        np.testing.assert_allclose(got[j], ref, atol=1e-12, rtol=0)
+    nb = -(-n // bs)
+    stride = F.block_bytes("bf16", bs, nkv, hd)
+    kc = np.zeros(nb * stride, np.uint8)
+    vc = np.zeros(nb * stride, np.uint8)
+    slots = np.arange(n)
+    cache_write("bf16", k.astype(np.float32), kc, slots, nkv, hd, bs, stride)
+    cache_write("bf16", v.astype(np.float32), vc, slots, nkv, hd, bs, stride)
+    tables = np.arange(nb)[None, :]
+    for window in (0, 5):
+        pd = paged_decode(q[None], kc, vc, tables, np.array([n]), nkv, hd, bs, stride, stride,
+                          "bf16", window=window)
+        lo = n - window if window else 0
+        np.testing.assert_array_equal(pd[0], attend(q, k[lo:], v[lo:]))
+    assert not attend(q, k[:0], v[:0]).any()
