@@ -217,11 +217,14 @@ def _compare(got, ref):
 
 
 def quality_report(ops, torch, ref_pools, pools, fmts, windows, q, tables, lens, nkv, bs, nseq,
-                   nq, hd, mb, k_scale, v_scale, wsp, in_dtype, dev, sparse=1e-3, reps=10):
+                   nq, hd, mb, k_scale, v_scale, wsp, in_dtype, dev, sparse=1e-3, reps=10,
+                   sample_seqs=(), samples=None):
     """Decode output of each format against the BF16-cache decode of the same
     K/V (unquantized attention; that kernel is within 2e-3 / 2e-4 of the fp64
     oracle in the parity tests), exact and with the sparse-V skip (weights
-    <= 1e-3 of the running sum dropped), and the sparse-V decode time."""
+    <= 1e-3 of the running sum dropped), and the sparse-V decode time.  The
+    output rows of the sequences in `sample_seqs` go to samples[(fmt,
+    window)] = (exact, sparse) for the comparison with the oracle."""
     rkp, rvp = ref_pools
     rep = {"reference": "bf16-cache decode of the same K/V"
                         + ("" if in_dtype == "bf16" else " (inputs rounded to bf16)"),
@@ -250,10 +253,127 @@ def quality_report(ops, torch, ref_pools, pools, fmts, windows, q, tables, lens,
             torch.cuda.synchronize()
             us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
             key = f if len(windows) == 1 else f"{f}@window{win}"
+            if samples is not None and sample_seqs:
+                idx = torch.tensor(list(sample_seqs), device=exact.device)
+                samples[(f, win)] = (exact[idx].double().cpu().numpy(),
+                                     sp[idx].double().cpu().numpy())
             rep[key] = {"exact": _compare(exact, ref),
                         "sparse_v": dict(_compare(sp, ref), vs_exact=_compare(sp, exact),
                                          us_per_layer=round(us, 2))}
     return rep
+
+
+def time_launches(torch, fn, reps, flush, stream):
+    """Median / min / p90 of `reps` CUDA-event-timed calls of fn on `stream`,
+    the L2 flushed (a read of more than it holds) before each call."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for e0, e1 in evs:
+        flush.sum()      # reads more than the L2 holds: clean lines, nothing to write back
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ts = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+    return {"median_us": statistics.median(ts), "min_us": ts[0],
+            "p90_us": ts[min(len(ts) - 1, (9 * len(ts)) // 10)], "launches": reps}
+
+
+def sample_sequences(lens):
+    """Sequences whose outputs the oracle recomputes: the shortest and the
+    longest (one of them if the batch is a single length), at most one of
+    more than 32768 positions."""
+    lens = np.asarray(lens)
+    if lens.size == 0:
+        return []
+    lo, hi = int(np.argmin(lens)), int(np.argmax(lens))
+    if lens[hi] > 32768 or lens[lo] == lens[hi]:
+        return [hi] if lens[hi] > 32768 else sorted({0, lens.size - 1})
+    return sorted({lo, hi})
+
+
+def host_rows(kall, vall, lens, seqs):
+    """fp32 host copies [L, nkv, hd] of the K and V rows of sequences `seqs`."""
+    starts = np.concatenate([[0], np.cumsum(np.asarray(lens, np.int64))])
+    return {s: (kall[int(starts[s]):int(starts[s + 1])].float().cpu().numpy(),
+                vall[int(starts[s]):int(starts[s + 1])].float().cpu().numpy()) for s in seqs}
+
+
+def measure_workload(args, name, dev, flush, reps, want_oracle, samples):
+    """Decode layers of another workload: each format's and window's layer
+    time (median of `reps` launches, L2 flushed before each), its quality
+    against the BF16-cache decode of the same K/V, and (for the oracle
+    comparison) the sampled sequences' inputs and outputs appended to
+    `samples`."""
+    import torch
+    from quantized_paged_kv_reshape_gb300 import ops, workloads as W
+
+    w = W.make(name)
+    nkv, nq, hd, bs, nseq = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size, w.num_seqs
+    lens_np = np.asarray(w.seq_lens, np.int64)
+    tables_np = W.block_tables(w)
+    mb = tables_np.shape[1]
+    tables = torch.from_numpy(tables_np).to(dev)
+    lens = torch.from_numpy(w.seq_lens).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4711)
+    ntok = int(lens_np.sum())
+    slots = torch.from_numpy(W.slot_mapping_for_sequences(w, tables_np)).to(dev)
+    ch_k = torch.from_numpy(W.channel_scales(w, 0)).to(dev)
+    ch_v = torch.from_numpy(W.channel_scales(w, 1)).to(dev)
+    kall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_k).to(torch.bfloat16)
+    vall = (torch.randn((ntok, nkv, hd), generator=g, device=dev) * ch_v).to(torch.bfloat16)
+    k_scale = float(kall.float().abs().amax()) / 448.0
+    v_scale = float(vall.float().abs().amax()) / 448.0
+    q = torch.randn((nseq, nq, hd), generator=g, device=dev).to(torch.bfloat16)
+    fmts, windows = list(w.formats), list(w.windows)
+    pools = {}
+    for f in fmts:
+        kp = ops.alloc_pool(w.num_blocks, f, 0, bs, nkv, hd, device=dev)
+        vp = ops.alloc_pool(w.num_blocks, f, 1, bs, nkv, hd, device=dev)
+        ops.cache_write(kall.view(ntok, -1), vall.view(ntok, -1), kp, vp, slots, f, nkv, hd, bs,
+                        k_scale=k_scale, v_scale=v_scale)
+        pools[f] = (kp, vp)
+    rkp = ops.alloc_pool(w.num_blocks, "bf16", 0, bs, nkv, hd, device=dev)
+    rvp = ops.alloc_pool(w.num_blocks, "bf16", 1, bs, nkv, hd, device=dev)
+    ops.cache_write(kall.view(ntok, -1), vall.view(ntok, -1), rkp, rvp, slots, "bf16", nkv, hd, bs)
+    seqs = sample_sequences(lens_np) if want_oracle else []
+    rows = host_rows(kall, vall, lens_np, seqs)
+    del kall, vall
+    wsp = {(f, win): ops.alloc_workspace(nseq, nq, nkv, hd, bs, mb, win, f, device=dev)
+           for f in fmts for win in windows}
+    out = torch.empty((nseq, nq, hd), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    peak, _ = peaks()
+    layers = {}
+    for f in fmts:
+        kp, vp = pools[f]
+        for win in windows:
+            def dec(f=f, kp=kp, vp=vp, win=win):
+                ops.paged_decode(q, kp, vp, tables, lens, f, nkv, bs, out=out, k_scale=k_scale,
+                                 v_scale=v_scale, sliding_window=win, workspace=wsp[(f, win)])
+            for _ in range(3):
+                dec()
+            m = time_launches(torch, dec, reps, flush, stream)
+            nbytes = algorithmic_decode_bytes(f, w.seq_lens, nkv, hd, bs, win)
+            gbs = nbytes / (m["median_us"] * 1e-6) / 1e9
+            key = f if len(windows) == 1 else f"{f}@window{win}"
+            layers[key] = {"us_per_layer": round(m["median_us"], 2), "decode_gbs": round(gbs, 1),
+                           "frac_of_peak": round(gbs / peak, 4), "cache_bytes": nbytes,
+                           "us_min": round(m["min_us"], 2), "us_p90": round(m["p90_us"], 2),
+                           "timing": f"median of {reps} launches, L2 flushed before each"}
+    got = {}
+    quality = quality_report(ops, torch, (rkp, rvp), pools, fmts, windows, q, tables, lens, nkv,
+                             bs, nseq, nq, hd, mb, k_scale, v_scale, wsp, "bf16", dev,
+                             sample_seqs=seqs, samples=got)
+    for (f, win), (ex, sp) in got.items():
+        for i, s in enumerate(seqs):
+            samples.append((name, f, win, s, q[s].double().cpu().numpy(), rows[s][0], rows[s][1],
+                            ex[i], sp[i]))
+    del pools, rkp, rvp, wsp
+    torch.cuda.empty_cache()
+    return {"config": WORKLOAD_DESC[name].format(nseq=nseq), "per_layer": layers,
+            "quality": quality}
 
 
 def run_gpu(args):
@@ -341,6 +461,9 @@ def run_gpu(args):
         ops.cache_write(kall.view(ntok, -1), vall.view(ntok, -1), rkp, rvp, slots_all, "bf16",
                         nkv, hd, bs)
         ref_pools = (rkp, rvp)
+    want_oracle = rank == 0 and not args.no_cpu_baseline and not args.no_quality
+    sample_seqs = sample_sequences(lens_np) if want_oracle else []
+    kv_samples = host_rows(kall, vall, lens_np, sample_seqs)
     del kall, vall
 
     stream = torch.cuda.current_stream()
@@ -444,6 +567,18 @@ def run_gpu(args):
     ms_total = t0.elapsed_time(t1)
     if ws > 1:
         torch.distributed.barrier()
+    # Per-layer figures: the median of `reps` launches of each decode layer,
+    # the L2 flushed before every launch.
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)   # 256 MB
+    reps = max(50, args.steps)
+    med = {key: time_launches(torch, fn, reps, flush, stream)
+           for kind, key, fn in calls if kind == "decode"}
+    # The other decode workloads of the same kind (one GPU only).
+    per_workload, extra_samples = {}, []
+    if ws == 1 and args.workload == "llama8b" and not args.no_extra and not args.num_seqs:
+        for name in ("ragged", "longctx"):
+            per_workload[name] = measure_workload(args, name, dev, flush, reps, want_oracle,
+                                                  extra_samples)
     clocks = sampler.stop() if rank == 0 else None
     ev = {key: [] for kind, key, _ in calls if kind == "decode"}
     evw = {key: [] for kind, key, _ in calls if kind == "write"}
@@ -491,9 +626,15 @@ def run_gpu(args):
     e2e_ms = s0.elapsed_time(s1) / e_steps
 
     ms_step, e2e_ms = slowest_rank([ms_total / args.steps, e2e_ms], dev)
+    main_samples = {}
     quality = quality_report(ops, torch, ref_pools, pools, fmts, windows, q, tables, lens, nkv,
-                             bs, nseq, nq, hd, mb, k_scale, v_scale, wsp, w.in_dtype, dev) \
+                             bs, nseq, nq, hd, mb, k_scale, v_scale, wsp, w.in_dtype, dev,
+                             sample_seqs=sample_seqs, samples=main_samples) \
         if ref_pools is not None else None
+    oracle_samples = [(args.workload, f, win, s, q[s].double().cpu().numpy(), kv_samples[s][0],
+                       kv_samples[s][1], main_samples[(f, win)][0][i], main_samples[(f, win)][1][i])
+                      for (f, win) in main_samples for i, s in enumerate(sample_seqs)]
+    oracle_samples += extra_samples
 
     dec_bytes = {(f, win): algorithmic_decode_bytes(f, w.seq_lens, nkv, hd, bs, win)
                  for f in fmts for win in windows}
@@ -503,11 +644,16 @@ def run_gpu(args):
     peak, peak_kind = peaks()
     per_layer = {}
     for (f, win), lst in ev.items():
-        us = statistics.mean(a.elapsed_time(b) for a, b in lst) * 1e3
+        us_step = statistics.mean(a.elapsed_time(b) for a, b in lst) * 1e3
+        m = med[(f, win)]
+        us = m["median_us"]
         gbs = dec_bytes[(f, win)] / (us * 1e-6) / 1e9
         key = f if len(windows) == 1 else f"{f}@window{win}"
         per_layer[key] = {"us_per_layer": round(us, 2), "decode_gbs": round(gbs, 1),
-                          "frac_of_peak": round(gbs / peak, 4), "cache_bytes": dec_bytes[(f, win)]}
+                          "frac_of_peak": round(gbs / peak, 4), "cache_bytes": dec_bytes[(f, win)],
+                          "timing": f"median of {m['launches']} launches, L2 flushed before each",
+                          "us_min": round(m["min_us"], 2), "us_p90": round(m["p90_us"], 2),
+                          "us_mean_in_step": round(us_step, 2)}
     full_size = not args.num_seqs or args.num_seqs == W.make(args.workload).num_seqs
     sm_hz = (clocks or {}).get("sm_mhz") or 0.0
     if full_size and sm_hz:
@@ -545,6 +691,7 @@ def run_gpu(args):
                    "parallelism": parallelism(ws),
                    "launch": launch_mode},
         "per_layer": per_layer,
+        "per_workload": per_workload or None,
         "cache_write": per_write,
         "roofline": {"kernel": f"decode_tc_kernel ({dom})", "bound": "hbm",
                      "achieved": per_layer[dom]["decode_gbs"], "peak": peak, "unit": "GB/s",
@@ -563,6 +710,8 @@ def run_gpu(args):
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+            if oracle_samples and line.get("quality") is not None:
+                line["quality"]["vs_oracle_fp64"] = oracle_quality(oracle_samples)
         print(json.dumps(line))
 
 
@@ -644,6 +793,39 @@ def oracle_on_host_cores(ntok, warmup, reps, seconds):
     total = sum(r[0] for r in res)
     per = sum(r[0] / r[1] for r in res) / procs
     return total / wall / 1e9, per / 1e9, procs, wall, res[0][2]
+
+
+def oracle_quality(samples, sparse=1e-3):
+    """Each format's GPU output rows of sampled sequences against the
+    oracle's fp64 attention over the original (bf16) K/V of those
+    sequences: max / mean |difference| and the cosine of each output row, for
+    the exact decode and for the one with the sparse-V skip."""
+    import oracle
+    acc = {}
+    for wname, fmt, win, s, q, k, v, ex, sp in samples:
+        lo = max(0, k.shape[0] - win) if win > 0 else 0
+        ref = oracle.attend(q, k[lo:], v[lo:])
+        key = f"{wname}:{fmt}" + (f"@window{win}" if wname == "longctx" else "")
+        a = acc.setdefault(key, {"exact": [], "sparse_v": [], "seqs": []})
+        a["seqs"].append(int(s))
+        for part, got in (("exact", ex), ("sparse_v", sp)):
+            d = np.abs(got - ref)
+            nr = np.linalg.norm(ref, axis=1)
+            cos = (got * ref).sum(axis=1) / np.maximum(np.linalg.norm(got, axis=1) * nr, 1e-300)
+            a[part].append((d.max(), d.sum(), d.size, cos[nr > 0]))
+    out = {"reference": "oracle fp64 attention on the original bf16 K/V of the sampled sequences",
+           "sparse_v_threshold": sparse}
+    for key, a in acc.items():
+        r = {"seqs": a["seqs"]}
+        for part in ("exact", "sparse_v"):
+            lst = a[part]
+            cos = np.concatenate([x[3] for x in lst]) if lst else np.zeros(0)
+            r[part] = {"max_abs": float(max(x[0] for x in lst)),
+                       "mean_abs": float(sum(x[1] for x in lst) / sum(x[2] for x in lst)),
+                       "cos_min": round(float(cos.min()), 6) if cos.size else None,
+                       "cos_mean": round(float(cos.mean()), 6) if cos.size else None}
+        out[key] = r
+    return out
 
 
 def cpu_baseline(seconds=15.0):
@@ -812,6 +994,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quality", action="store_true",
                     help="skip the quality report against a BF16 cache of the same K/V")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the ragged and long-context decode layers of the llama8b run")
     ap.add_argument("--graphs", action="store_true",
                     help="time per-call CUDA graph replays instead of direct calls")
     ap.add_argument("--num-seqs", type=int, default=0, help="override the number of sequences")

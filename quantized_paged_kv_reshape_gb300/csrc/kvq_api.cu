@@ -437,7 +437,8 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype q_dtype, int64_t q_stride, 
   a.out_bf16 = out_dtype == KVQ_DTYPE_BF16;
   a.err = error_flag;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_decode_tc(ks, vs, hd, a, cb, st);
+  cudaError_t e = decode_tma_supported(ks, vs, hd, nkv, bs) ? launch_decode_tma(ks, vs, hd, a, cb, st)
+                                                            : launch_decode_tc(ks, vs, hd, a, cb, st);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -1,0 +1,19 @@
+// TMA-fed decode instances whose K side is T4 (one translation unit per K
+// side so the instances compile in parallel).  V sides: the catalogue's
+// pairs with this K side ("spark_runtime/kv_cache.rs", KvCacheDtype::kv_pair)
+// that the TMA decode handles.
+#include "kvq_decode_tma.cuh"
+
+namespace kvq {
+
+cudaError_t launch_tma_k_t4(int v_side, int hd, const DecodeArgs& a, const TmaMaps& maps,
+                              const Codebooks& cb, cudaStream_t st) {
+  switch (v_side) {
+    case S_T4: return hd == 64 ? launch_tma_inst<S_T4, S_T4, 64>(a, maps, cb, st)
+                             : launch_tma_inst<S_T4, S_T4, 128>(a, maps, cb, st);
+    case S_T3: return hd == 128 ? launch_tma_inst<S_T4, S_T3, 128>(a, maps, cb, st) : cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvq

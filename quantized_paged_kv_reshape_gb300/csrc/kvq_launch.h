@@ -99,6 +99,17 @@ cudaError_t launch_tc_k_t2(int v_side, int hd, const DecodeArgs&, const Codebook
 cudaError_t launch_tc_k_t8(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 cudaError_t launch_tc_k_nvfp4(int v_side, int hd, const DecodeArgs&, const Codebooks&, cudaStream_t);
 
+// TMA-fed decode (kvq_decode_tma_*.cu) for the sides, head dims and
+// shapes it handles; the others run decode_tc_kernel.
+struct TmaMaps;
+bool decode_tma_supported(int k_side, int v_side, int hd, int nkv, int bs);
+cudaError_t launch_decode_tma(int k_side, int v_side, int hd, const DecodeArgs& a,
+                              const Codebooks& cb, cudaStream_t st);
+cudaError_t launch_tma_k_bf16(int v_side, int hd, const DecodeArgs&, const TmaMaps&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tma_k_fp8(int v_side, int hd, const DecodeArgs&, const TmaMaps&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tma_k_t4(int v_side, int hd, const DecodeArgs&, const TmaMaps&, const Codebooks&, cudaStream_t);
+cudaError_t launch_tma_k_nvfp4(int v_side, int hd, const DecodeArgs&, const TmaMaps&, const Codebooks&, cudaStream_t);
+
 // Chunked prefill (kvq_prefill_k_*.cu), same pairs as the decode.
 cudaError_t launch_pf_k_bf16(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);
 cudaError_t launch_pf_k_fp8(int v_side, int hd, const PrefillArgs&, const Codebooks&, int, cudaStream_t);

@@ -17,6 +17,17 @@ from quantized_paged_kv_reshape_gb300 import ops
 pytestmark = pytest.mark.gpu
 
 LENS = [37, 50, 1, 0, 16, 300, 129]
+TMA_FORMATS = ["bf16", "fp8", "nvfp4", "turbo4", "turbo4k_turbo3v", "bf16k_turbo4v",
+               "bf16k_turbo3v", "fp8k_turbo4v", "fp8k_turbo3v", "bf16k_turbo2v", "fp8k_turbo2v"]
+
+
+@pytest.fixture(params=["auto", "mma"], autouse=True)
+def decode_kernel(request, monkeypatch):
+    """Every test runs with the library's own kernel choice (the TMA-fed
+    kernel where the sides and shape allow it) and with the mma.sync kernel
+    forced for every call."""
+    monkeypatch.setenv("KVQ_DECODE_KERNEL", request.param)
+    return request.param
 
 
 @pytest.mark.parametrize("fmt", ALL_FORMATS)
@@ -30,6 +41,26 @@ def test_decode_parity(fmt, hd, nq, nkv):
     ref = oracle_decode(c)
     assert_decode_close(got, ref)
     assert not got[:, :, :][3].any()          # seq_len 0 -> zero row
+
+
+@pytest.mark.parametrize("fmt", TMA_FORMATS)
+@pytest.mark.parametrize("hd,nq,nkv", [(64, 16, 4), (64, 64, 8), (128, 16, 4), (128, 64, 8),
+                                       (128, 24, 8)])
+def test_decode_wide_heads(fmt, hd, nq, nkv):
+    """Shapes whose scale rows the TMA copies per 16-byte span (four or more
+    kv heads at head_dim 64), GQA 8 and GQA 3 with eight kv heads."""
+    c = decode_case(fmt, [300, 1, 0, 47, 129, 16], nq, nkv, hd, seed=hd + nq + nkv)
+    assert_decode_close(gpu_decode(c), oracle_decode(c))
+
+
+@pytest.mark.parametrize("bs", [8, 32])
+@pytest.mark.parametrize("fmt", ["turbo4", "bf16k_turbo3v", "fp8k_turbo2v", "nvfp4"])
+def test_decode_block_sizes_windows(bs, fmt):
+    """Block sizes 8 and 32 with windows that start inside a slab and inside
+    a page."""
+    c = decode_case(fmt, [70, 9, 257, 1, 33], 32, 8, 128, bs=bs, seed=bs + 1)
+    for window in (0, 3, 17, 40):
+        assert_decode_close(gpu_decode(c, window=window), oracle_decode(c, window=window))
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "turbo4k_turbo3v", "fp8k_turbo2v", "turbo8"])
