@@ -667,12 +667,38 @@ def run_gpu(args):
                               "peak_ginst_s": round(issue_peak / 1e9, 1),
                               "frac": round(rate / issue_peak, 4)}
     per_write = {}
+    # The step's write on its own: a CUDA graph of 20 back-to-back calls,
+    # replayed, so that host launch gaps do not count (a single small write
+    # bracketed by events also measures how long the GPU waited for the host
+    # to enqueue it).
+    write_gpu_us = {}
+    for kind, key, fn in calls:
+        if kind != "write":
+            continue
+        try:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                for _ in range(20):
+                    fn()
+            gr.replay()
+            torch.cuda.synchronize()
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for _ in range(5):
+                gr.replay()
+            g1.record(stream)
+            torch.cuda.synchronize()
+            write_gpu_us[key] = g0.elapsed_time(g1) * 1e3 / 100
+            del gr
+        except RuntimeError:
+            torch.cuda.synchronize()
     for f in fmts:
         wms = statistics.mean(write_ms[f])
         us_w = statistics.mean(a.elapsed_time(b) for a, b in evw[f]) * 1e3
         per_write[f] = {"fill_gbs": round(write_bytes(f, ntok, nkv, hd, bs, in_bytes) / (wms * 1e-3) / 1e9, 1),
                         "fill_us": round(wms * 1e3, 1), "fill_tokens": ntok,
                         "step_write_us": round(us_w, 2), "step_write_tokens": wtok,
+                        "step_write_gpu_us": round(write_gpu_us[f], 2) if f in write_gpu_us else None,
                         "step_write_gbs": round(write_bytes(f, wtok, nkv, hd, bs, in_bytes) / (us_w * 1e-6) / 1e9, 1)}
     dom = max(per_layer, key=lambda k: per_layer[k]["us_per_layer"])
     value = job_rate(step_bytes, ws, ms_step)

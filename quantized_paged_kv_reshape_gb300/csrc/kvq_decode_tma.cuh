@@ -264,8 +264,16 @@ struct TmCfg {
   static constexpr int HEAD = align_up(OFF_BAR + 64 * 8, 1024);
   static constexpr int LUT_OFF = LUT ? kLutAddr - kSmemBase : 0;   // from the dynamic base
   static constexpr int LUT_END = LUT ? LUT_OFF + 0x10000 : 0;
-  static constexpr int MERGE_BYTES = 16 * 8 * HD * 4 + 16 * 8 * 2 * 4;
+  static constexpr int MERGE_BYTES = 16 * 8 * HD * 4 + 16 * 8 * 2 * 4;   // (for 16 warps)
 
+  // CTAs per SM (measured on GB300, llama8b layer): FP8 runs two CTAs of 8
+  // warps, whose unit boundaries (merge, next unit's first copies) then
+  // overlap each other's streaming (59.9 against 65.5 us with one CTA of 16);
+  // BF16 one CTA of 8 warps (94.3 against 98.3 us with two of 4); the sides
+  // with code tables one CTA, whose fixed table placement needs the whole of
+  // it.
+  static constexpr int CPS = (!LUT && KS == S_FP8) ? 2 : 1;
+  static constexpr int LIMIT = CPS == 1 ? kSmemLimit : (228 * 1024) / CPS - 1024;
   static constexpr TmLayout layout(int nw, int nst) {
     const int sz[4] = {nw * nst * K::TILE, nw * nst * V::TILE, nw * nst * K::STILE,
                        nw * nst * V::STILE};
@@ -292,9 +300,11 @@ struct TmCfg {
     int end = a > b ? a : b;
     if (LUT && end < LUT_END) end = LUT_END;
     if (mg + MERGE_BYTES > end) end = mg + MERGE_BYTES;
-    return TmLayout{off[0], off[1], off[2], off[3], mg, end, end <= kSmemLimit};
+    return TmLayout{off[0], off[1], off[2], off[3], mg, end, end <= LIMIT};
   }
-  static constexpr int pick_nw() { return layout(16, 3).ok ? 16 : 8; }
+  static constexpr int pick_nw() {
+    return CPS == 1 ? (layout(16, 3).ok ? 16 : 8) : (layout(8, 3).ok ? 8 : 4);
+  }
   static constexpr int NW = pick_nw();
   static constexpr int pick_nst() {
     return layout(NW, 4).ok ? 4 : layout(NW, 3).ok ? 3 : 2;
@@ -327,7 +337,7 @@ __device__ __forceinline__ int tm_v_row_dim(int i, int row) {
 }
 
 template <int KS, int VS, int HD, bool PK>
-__global__ void __launch_bounds__(32 * TmCfg<KS, VS, HD>::NW, 1)
+__global__ void __launch_bounds__(32 * TmCfg<KS, VS, HD>::NW, TmCfg<KS, VS, HD>::CPS)
 decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, const Codebooks cb) {
   using C = TmCfg<KS, VS, HD>;
   using KT = typename C::K;
@@ -501,52 +511,56 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
   // two of 8 (block_size 8); a piece outside the attended range or whose
   // block id is invalid is not copied.
   bool dirty = true;      // a stage holds generic-proxy writes the copies must follow
-  auto issue = [&](int s) {
-    if (lane != 0) return;
-    const uint32_t st = (gk + (uint32_t)s) % NST;
+  auto issue = [&](int s, uint32_t st) {
+    // Every lane computes the same operands (the block ids are broadcast
+    // from lane 0), so that the copies' operands are warp-uniform; lane 0
+    // issues.
     const uint32_t bar = bar0 + st * 8;
     const int slab_pos = tok0 + (warp + NW * s) * SLAB;
-    const int rows = bs < 16 ? bs : 16;
-    const int npiece = SLAB / rows;
-    int blk[2] = {-1, -1};
-    uint32_t bytes = 0;
-    for (int p = 0; p < npiece; ++p) {
-      const int pos = slab_pos + p * rows;
-      if (pos + rows > lo && pos < tok_end) blk[p] = blk_s[(pos >> lbs) - p0];
-      if (blk[p] >= 0) bytes += rows * C::ROWBYTES;
+    int b0 = -1, b1 = -1;
+    if (bs >= 16) {   // one page holds the slab, and the slab meets [lo, tok_end)
+      b0 = blk_s[(slab_pos >> lbs) - p0];
+    } else {          // two pages of 8 positions; a page outside [lo, tok_end) is skipped
+      if (slab_pos + 8 > lo) b0 = blk_s[(slab_pos >> lbs) - p0];
+      if (slab_pos + 8 < tok_end) b1 = blk_s[((slab_pos + 8) >> lbs) - p0];
     }
-    if (dirty) {   // generic writes (cleared rows, merge scratch) before the copies' writes
-      tm::fence_async();
-      dirty = false;
+    b0 = __shfl_sync(0xffffffffu, b0, 0);
+    b1 = __shfl_sync(0xffffffffu, b1, 0);
+    const int rows = bs < 16 ? 8 : 16;
+    const uint32_t bytes = (uint32_t)(((b0 >= 0) + (b1 >= 0)) * rows * C::ROWBYTES);
+    const int in_page = slab_pos & (bs - 1);
+    if (lane == 0) {
+      if (dirty) tm::fence_async();   // generic writes (cleared rows, merge scratch) first
+      if (bytes == 0) {
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+      } else {
+        tm::bar_expect(bar, bytes);
+      }
     }
-    if (bytes == 0) {
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-      return;
-    }
-    tm::bar_expect(bar, bytes);
-    for (int p = 0; p < npiece; ++p) {
-      if (blk[p] < 0) continue;
-      const int pos = slab_pos + p * rows;
-      const int in_page = pos & (bs - 1);
+    dirty = false;
+    auto piece = [&](int p, int blk, int ip) {
+      if (lane != 0 || blk < 0) return;
 #pragma unroll
       for (int b = 0; b < KT::NBOX; ++b)
-        tm::tma4(rkd + st * KT::TILE + b * 16 * KT::BOXW + p * rows * KT::BOXW, &maps.kd, b * KT::BOXW,
-                 kvh, in_page, blk[p], bar);
+        tm::tma4(rkd + st * KT::TILE + b * 16 * KT::BOXW + p * 8 * KT::BOXW, &maps.kd, b * KT::BOXW,
+                 kvh, ip, blk, bar);
 #pragma unroll
       for (int b = 0; b < VT::NBOX; ++b)
-        tm::tma4(rvd + st * VT::TILE + b * 16 * VT::BOXW + p * rows * VT::BOXW, &maps.vd, b * VT::BOXW,
-                 kvh, in_page, blk[p], bar);
+        tm::tma4(rvd + st * VT::TILE + b * 16 * VT::BOXW + p * 8 * VT::BOXW, &maps.vd, b * VT::BOXW,
+                 kvh, ip, blk, bar);
       if constexpr (KT::SROW > 0) {
-        const uint32_t d = rks + st * KT::STILE + p * rows * KT::SBOXW;
-        if constexpr (KT::SROW >= 16) tm::tma4(d, &maps.ks, 0, kvh, in_page, blk[p], bar);
-        else tm::tma3(d, &maps.ks, (kvh * KT::SROW) & ~15, in_page, blk[p], bar);
+        const uint32_t d = rks + st * KT::STILE + p * 8 * KT::SBOXW;
+        if constexpr (KT::SROW >= 16) tm::tma4(d, &maps.ks, 0, kvh, ip, blk, bar);
+        else tm::tma3(d, &maps.ks, (kvh * KT::SROW) & ~15, ip, blk, bar);
       }
       if constexpr (VT::SROW > 0) {
-        const uint32_t d = rvs + st * VT::STILE + p * rows * VT::SBOXW;
-        if constexpr (VT::SROW >= 16) tm::tma4(d, &maps.vs, 0, kvh, in_page, blk[p], bar);
-        else tm::tma3(d, &maps.vs, (kvh * VT::SROW) & ~15, in_page, blk[p], bar);
+        const uint32_t d = rvs + st * VT::STILE + p * 8 * VT::SBOXW;
+        if constexpr (VT::SROW >= 16) tm::tma4(d, &maps.vs, 0, kvh, ip, blk, bar);
+        else tm::tma3(d, &maps.vs, (kvh * VT::SROW) & ~15, ip, blk, bar);
       }
-    }
+    };
+    piece(0, b0, in_page);
+    if (bs < 16) piece(1, b1, (slab_pos + 8) & (bs - 1));
   };
 
   // ---- per-thread constants of the fragment loads
@@ -942,7 +956,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       if (tid == 0) st[5] = sa + nsl;
       const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
       dirty = true;   // the merge of the previous unit wrote over the rings
-      for (int s = 0; s < NST && s < my; ++s) issue(s);
+      for (int s = 0; s < NST && s < my; ++s) issue(s, (gk + (uint32_t)s) % NST);
       if (first_stretch) {
         // ---- queries (rotated when K is stored rotated), rows >= rep zero
         for (int j = warp; j < 8; j += NW) {
@@ -1003,7 +1017,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
         }
         if (bad == 0xffffu) {   // nothing to attend here
           __syncwarp();
-          if (s + NST < my) issue(s + NST);
+          if (s + NST < my) issue(s + NST, stg);
           continue;
         }
         if (bad) {
@@ -1062,7 +1076,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
         }
         if (pv_any) pv(stg, pw[0], pw[1], pw[2], pw[3]);
         __syncwarp();
-        if (s + NST < my) issue(s + NST);
+        if (s + NST < my) issue(s + NST, stg);
       }
       if (failed) {
         // copies of this stretch still in flight: wait for them (bounded)
@@ -1236,7 +1250,7 @@ cudaError_t launch_tma_kern(const DecodeArgs& a, const TmaMaps& maps, const Code
     if (e != cudaSuccess) return e;
     attr_dev = dev;
   }
-  const int ranges = max(1, min(a.max_ranges, a.sms / a.nkv));
+  const int ranges = max(1, min(a.max_ranges, C::CPS * a.sms / a.nkv));
   kern<<<ranges * a.nkv, 32 * C::NW, C::SMEM, st>>>(a, maps, cb);
   return cudaGetLastError();
 }
