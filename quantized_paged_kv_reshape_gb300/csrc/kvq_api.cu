@@ -145,6 +145,18 @@ const Codebooks& codebooks() {
         out[k][1] = thr;
       }
     };
+    // The cache write's Turbo4/3 search buckets quotients by fmaf(v, 4, 2^20 +
+    // 128.5) rounded to eighths: edges (k - 128.5) / 4 blur by up to 1/64, so
+    // no threshold may lie that close to one.
+    auto check_edges = [](const float* th, int n) {
+      for (int i = 0; i < n; ++i) {
+        const double e = std::floor(4.0 * th[i] + 128.5) - 128.5;
+        const double d = std::fmin(std::fabs(th[i] - e / 4.0), std::fabs(th[i] - (e + 1.0) / 4.0));
+        if (d < 1.0 / 48) std::abort();   // the blur is 1/64; Turbo4 keeps 0.0257
+      }
+    };
+    check_edges(g_cb.th4, 15);
+    check_edges(g_cb.th3, 7);
     buckets(g_cb.th4, 15, g_cb.bucket[0]);
     buckets(g_cb.th3, 7, g_cb.bucket[1]);
     buckets(g_cb.th2, 3, g_cb.bucket[2]);
@@ -205,6 +217,28 @@ size_t workspace_need(int num_seqs, int nq, int nkv, int hd, const DecodePlan& p
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// 1/x where x is a power of two whose reciprocal is a normal float (then x *
+// (1/x) rounds exactly like a division by x), else 0.
+float exact_reciprocal(float x) {
+  int e = 0;
+  const float m = std::frexp(x, &e);
+  if (!(x > 0.f) || !std::isfinite(x) || m != 0.5f) return 0.f;
+  const float r = 1.0f / x;
+  return (std::isnormal(r) && r * x == 1.0f) ? r : 0.f;
+}
+
+// Multiplier and shifts of Granlund and Montgomery's round-up division by d
+// ("Division by invariant integers using multiplication", 1994, Figure 4.1):
+// with l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, every 32-bit n
+// gives n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0), t = umulhi(m, n).
+void set_fast_div(uint32_t d, uint32_t& m, uint32_t& s1, uint32_t& s2) {
+  uint32_t l = 0;
+  while (l < 32 && ((uint64_t)1 << l) < d) ++l;
+  m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << l) - d)) / d + 1);
+  s1 = l < 1 ? l : 1;
+  s2 = l > 1 ? l - 1 : 0;
+}
 
 int rmax_for(int rep) { return rep <= 1 ? 1 : rep <= 2 ? 2 : rep <= 4 ? 4 : rep <= 8 ? 8 : 0; }
 
@@ -314,12 +348,10 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
   const Codebooks& cb = codebooks();
   const bool bf = in_dtype == KVQ_DTYPE_BF16;
   const int el = bf ? 2 : 4;
-  // bytes of one lane's vector load: a row takes 16 lanes (head_dim 64/128)
-  // or 32 (256), head_dim / lanes elements each
-  const int lanes = hd == 256 ? 32 : 16;
-  const int va = bf ? (hd / lanes) * 2 : 8;
-  const bool vec = ((uintptr_t)key % va == 0) && ((uintptr_t)value % va == 0) &&
-                   (key_stride * el) % va == 0 && (value_stride * el) % va == 0;
+  // every lane loads 16 consecutive elements (one scale group) as 16-byte
+  // vectors: the rows' starts must keep that alignment
+  const bool vec = aligned16(key) && aligned16(value) && (key_stride * el) % 16 == 0 &&
+                   (value_stride * el) % 16 == 0;
   WriteArgs a{};
   a.key = key;
   a.value = value;
@@ -339,17 +371,14 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
   a.v_dsec = kvq_data_section_bytes(fmt, 1, bs, nkv, hd);
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.k_inv = exact_reciprocal(k_scale);
+  a.v_inv = exact_reciprocal(v_scale);
   a.inv_sqrt_hd = (float)(1.0 / std::sqrt((double)hd));
   a.k_side = ks;
   a.v_side = vs;
+  set_fast_div((uint32_t)nkv, a.nkv_m, a.nkv_s1, a.nkv_s2);
   a.err = error_flag;
-  // units = (token pair or token, side, kv head): 32 / lanes rows each
-  const int64_t units = ((int64_t)num_tokens + 32 / lanes - 1) / (32 / lanes) * nkv * 2;
-  const int sms = sm_count();
-  const int64_t want = (units + 15) / 16;   // 8 warps x 2 units per CTA iteration
-  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 32;
-  const int grid = (int)(want < cap ? want : cap);
-  cudaError_t e = launch_cache_write(a, cb, hd, bf, vec, grid, (cudaStream_t)stream);
+  cudaError_t e = launch_cache_write(a, cb, hd, bf, vec, sm_count(), (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(KVQ_ERR_CUDA, "cache write launch: %s", cudaGetErrorString(e));
   return ok();
 }

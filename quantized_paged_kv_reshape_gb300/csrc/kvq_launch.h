@@ -25,8 +25,12 @@ struct WriteArgs {
   int64_t k_bstride, v_bstride;         // bytes per block
   int64_t k_dsec, v_dsec;               // scale-section offsets
   float k_scale, v_scale;               // per-tensor FP8 scales
+  float k_inv, v_inv;                   // 1/scale where scale is a power of two, else 0
   float inv_sqrt_hd;                    // fp32(1/sqrt(head_dim))
   int k_side, v_side;
+  // n / nkv for n < 2^31 as (h + ((n - h) >> nkv_s1)) >> nkv_s2, h =
+  // umulhi(n, nkv_m) (Granlund and Montgomery's round-up division)
+  uint32_t nkv_m, nkv_s1, nkv_s2;
   int32_t* err;
 };
 
@@ -85,7 +89,7 @@ struct PrefillArgs {  // arguments of the chunked prefill (prefill_tc5_kernel)
 };
 
 cudaError_t launch_cache_write(const WriteArgs& a, const Codebooks& cb, int head_dim,
-                               bool in_bf16, bool vec, int grid, cudaStream_t st);
+                               bool in_bf16, bool vec, int sms, cudaStream_t st);
 
 // Tensor-core decode (kvq_decode_tc_k_*.cu) for the pairs it supports.
 bool decode_tc_supported(int k_side, int v_side);

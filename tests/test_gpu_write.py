@@ -207,3 +207,74 @@ def test_write_graph_replay():
         oracle.cache_write(vside, v, vc, slots, nkv, hd, bs, vst)
         assert np.array_equal(kpool.cpu().numpy().reshape(-1), kc)
         assert np.array_equal(vpool.cpu().numpy().reshape(-1), vc)
+
+
+def _write_pair(fmt, k, v, slots, nkv, hd, bs, num_blocks, ks=1.0, vs=1.0, in_dtype="f32"):
+    """Oracle bytes and GPU bytes of one write of K rows k and V rows v."""
+    kside, vside = oracle.kv_pair(fmt)
+    kst = (oracle.block_bytes(kside, bs, nkv, hd) + 15) // 16 * 16
+    vst = (oracle.block_bytes(vside, bs, nkv, hd) + 15) // 16 * 16
+    kc = np.zeros(num_blocks * kst, np.uint8)
+    vc = np.zeros(num_blocks * vst, np.uint8)
+    oracle.cache_write(kside, k, kc, slots, nkv, hd, bs, kst, scale=ks)
+    oracle.cache_write(vside, v, vc, slots, nkv, hd, bs, vst, scale=vs)
+    tdt = torch.bfloat16 if in_dtype == "bf16" else torch.float32
+    ntok = k.shape[0]
+    kd = torch.from_numpy(k.reshape(ntok, -1)).cuda().to(tdt)
+    vd = torch.from_numpy(v.reshape(ntok, -1)).cuda().to(tdt)
+    kpool = torch.zeros((num_blocks, kst), dtype=torch.uint8, device="cuda")
+    vpool = torch.zeros((num_blocks, vst), dtype=torch.uint8, device="cuda")
+    ops.cache_write(kd, vd, kpool, vpool, torch.from_numpy(slots).cuda(), fmt, nkv, hd, bs,
+                    k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    return kc, vc, kpool.cpu().numpy().reshape(-1), vpool.cpu().numpy().reshape(-1)
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hd", [64, 128, 256])
+@pytest.mark.parametrize("fmt", ["turbo4", "turbo3", "turbo2", "nvfp4", "turbo8",
+                                 "turbo4k_turbo3v", "bf16k_turbo2v"])
+def test_write_extreme_magnitudes(fmt, hd, in_dtype):
+    """Rows scaled so that group scales saturate at E4M3's 448 (the quotients
+    then run far past the top level), land in E4M3's subnormal range or round
+    to zero, all-zero rows, -0 elements and lone spikes: bytes equal the
+    oracle's."""
+    rng = np.random.default_rng(hd + (7 if in_dtype == "bf16" else 0))
+    nkv, bs = 2, 16
+    factors = np.array([3e5, 2e3, 1.0, 1e-3, 3e-5, 1e-7, 1e-30, 0.0], np.float32)
+    ntok = 2 * len(factors)
+    k = rng.standard_normal((ntok, nkv, hd)).astype(np.float32)
+    v = rng.standard_normal((ntok, nkv, hd)).astype(np.float32)
+    for t in range(ntok):
+        k[t] *= factors[t % len(factors)]
+        v[t] *= factors[(t + 3) % len(factors)]
+    k[1, 0, :] = -0.0                                   # a row of -0
+    v[2, 1, ::3] = -0.0                                 # -0 elements among values
+    k[5, 1, :] = 0.0
+    k[5, 1, 17] = -4e4                                  # a lone spike
+    v[6, 0, :] = 1e-3
+    v[6, 0, 40] = 9e3
+    if in_dtype == "bf16":
+        k, v = bf16_round(k), bf16_round(v)
+    slots = rng.permutation(ntok).astype(np.int64)
+    kc, vc, kg, vg = _write_pair(fmt, k, v, slots, nkv, hd, bs, 1, in_dtype=in_dtype)
+    assert np.array_equal(kc, kg), f"K bytes differ at {np.flatnonzero(kc != kg)[:8]}"
+    assert np.array_equal(vc, vg), f"V bytes differ at {np.flatnonzero(vc != vg)[:8]}"
+
+
+@pytest.mark.parametrize("scales", [(1.0, 0.25), (3.0, 0.37), (2.0 ** -20, 2.0 ** 20)])
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_write_fp8_scales(hd, scales):
+    """FP8 codes of x / scale: powers of two (a product with the exact
+    reciprocal) and other scales (a division) round like the oracle's fp32
+    division, saturating at 448."""
+    rng = np.random.default_rng(hd)
+    nkv, bs, ntok = 3, 16, 21
+    ks, vs = scales
+    k = (rng.standard_normal((ntok, nkv, hd)) * 40 * ks).astype(np.float32)
+    v = (rng.standard_normal((ntok, nkv, hd)) * 40 * vs).astype(np.float32)
+    k[0, 0, :4] = [1e30, -1e30, -0.0, 0.0]
+    slots = rng.permutation(2 * bs)[:ntok].astype(np.int64)
+    kc, vc, kg, vg = _write_pair("fp8", k, v, slots, nkv, hd, bs, 2, ks=ks, vs=vs)
+    assert np.array_equal(kc, kg), f"K bytes differ at {np.flatnonzero(kc != kg)[:8]}"
+    assert np.array_equal(vc, vg), f"V bytes differ at {np.flatnonzero(vc != vg)[:8]}"
