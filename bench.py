@@ -60,9 +60,9 @@ WORKLOAD_DESC = {
 # decode launch, from the ncu capture summarised in profiles/ (None when the
 # kernel changed after the capture).
 TRAFFIC = {
-    ("llama8b", "bf16"): 541_548_288,
-    ("llama8b", "fp8"): 270_268_416,
-    ("llama8b", "turbo4"): 152_777_216,
+    ("llama8b", "bf16"): 541_241_856,
+    ("llama8b", "fp8"): 269_910_272,
+    ("llama8b", "turbo4"): 153_706_752,
 }
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # prefill launch (the slowest format of the workload), from the 1-pass ncu
@@ -80,9 +80,9 @@ PF_TRAFFIC = {
 # peak = 4 warp-instructions per cycle per SM (one per sub-partition) x the
 # SMs x the SM clock sampled during the timed region.
 WARP_INSTR = {
-    ("llama8b", "bf16"): 25_501_653,
-    ("llama8b", "fp8"): 29_071_653,
-    ("llama8b", "turbo4"): 64_988_213,
+    ("llama8b", "bf16"): 20_692_773,
+    ("llama8b", "fp8"): 25_321_929,
+    ("llama8b", "turbo4"): 49_975_176,
 }
 
 
@@ -724,7 +724,7 @@ def run_gpu(args):
         "per_layer": per_layer,
         "per_workload": per_workload or None,
         "cache_write": per_write,
-        "roofline": {"kernel": f"decode_tc_kernel ({dom})", "bound": "hbm",
+        "roofline": {"kernel": f"{ops.decode_kernel(dom_fmt, hd, nkv, bs)} ({dom})", "bound": "hbm",
                      "achieved": per_layer[dom]["decode_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": round(per_layer[dom]["decode_gbs"] / peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind + " (hbm_gbs copy)",

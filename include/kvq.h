@@ -188,6 +188,18 @@ kvq_status kvq_cache_write(
 
 /* ------------------------------------------------------------ paged decode */
 
+/* Which decode kernel kvq_paged_decode launches on the current device for
+ * these arguments: 1 = the kernel that stages cache pages with TMA tensor
+ * copies (BF16/FP8/Turbo4/NVFP4 K sides, head_dim 64/128), 0 = the kernel
+ * that stages them with cp.async (every other case, and every case when the
+ * environment variable KVQ_DECODE_KERNEL is "mma"), -1 = a format, head_dim,
+ * num_kv_heads or block_size kvq_paged_decode rejects.  Both compute the
+ * same attention ("combs_models/kv.rs", attend; "spark_runtime/kv_cache.rs",
+ * is_wht_rotated).  Host only; no device work. */
+int32_t kvq_decode_path(kvq_format fmt, int32_t head_dim, int32_t num_kv_heads,
+                        int32_t block_size);
+
+
 /* Bytes of device scratch kvq_paged_decode needs for these arguments: fp32
  * partial results of (sequence, query head) rows that several CTAs share,
  * followed by one int32 merge counter per (sequence, kv head) (the last

@@ -51,6 +51,7 @@ _SIGS = {
         C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
         C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_int64,
         C.c_int64, C.c_int64, C.c_float, C.c_float, C.c_int, C.c_void_p, C.c_void_p]),
+    "kvq_decode_path": (C.c_int32, [C.c_int, C.c_int32, C.c_int32, C.c_int32]),
     "kvq_decode_workspace_bytes": (C.c_size_t, [
         C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int]),
     "kvq_paged_decode": (C.c_int, [
@@ -141,6 +142,10 @@ def kvq_cache_write(key, value, in_dtype, k_cache, v_cache, slot_mapping, num_to
         key, value, in_dtype, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
         num_kv_heads, head_dim, block_size, key_stride, value_stride, k_block_stride_bytes,
         v_block_stride_bytes, k_scale, v_scale, int(fmt), error_flag, stream))
+
+
+def kvq_decode_path(fmt, head_dim, num_kv_heads, block_size):
+    return lib().kvq_decode_path(int(fmt), head_dim, num_kv_heads, block_size)
 
 
 def kvq_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,

@@ -383,6 +383,13 @@ kvq_status kvq_cache_write(const void* key, const void* value, kvq_dtype in_dtyp
   return ok();
 }
 
+int32_t kvq_decode_path(kvq_format fmt, int32_t hd, int32_t nkv, int32_t bs) {
+  if (!fmt_ok(fmt) || (hd != 64 && hd != 128 && hd != 256) || nkv < 1 ||
+      (bs != 8 && bs != 16 && bs != 32))
+    return -1;
+  return decode_tma_supported(side_of(fmt, 0), side_of(fmt, 1), hd, nkv, bs) ? 1 : 0;
+}
+
 size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t nq, int32_t nkv, int32_t hd, int32_t bs,
                                   int32_t max_blocks, int32_t window, kvq_format fmt) {
   if (!fmt_ok(fmt) || num_seqs < 0 || nq < 1 || nkv < 1 || hd < 1 || bs < 1 || max_blocks < 1 ||

@@ -67,6 +67,15 @@ def cache_write(key, value, k_cache, v_cache, slot_mapping, fmt, num_kv_heads, h
         _stream_ptr(stream))
 
 
+def decode_kernel(fmt, head_dim, num_kv_heads, block_size):
+    """Name of the decode kernel paged_decode launches on the current device
+    for these arguments ("decode_tma_kernel" or "decode_tc_kernel")."""
+    p = A.kvq_decode_path(fmt_id(fmt), head_dim, num_kv_heads, block_size)
+    if p < 0:
+        raise ValueError("arguments the decode rejects")
+    return "decode_tma_kernel" if p == 1 else "decode_tc_kernel"
+
+
 def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            max_blocks_per_seq, sliding_window, fmt):
     return A.kvq_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,

@@ -178,3 +178,15 @@ def test_workspace_formula():
     n = A.kvq_decode_workspace_bytes(32, 32, 8, 128, 16, 256, 40, 0)
     assert n == 2 * row + counts
     assert A.kvq_decode_workspace_bytes(32, 32, 8, 128, 24, 256, 0, 0) == 0
+
+
+def test_decode_path_rejects_what_the_decode_rejects():
+    """kvq_decode_path answers -1 for arguments kvq_paged_decode refuses (no
+    device work, so it runs without a GPU)."""
+    from quantized_paged_kv_reshape_gb300 import _abi as A, ops
+    t4 = ops.fmt_id("turbo4")
+    assert A.kvq_decode_path(t4, 96, 8, 16) == -1      # head_dim
+    assert A.kvq_decode_path(t4, 128, 0, 16) == -1     # num_kv_heads
+    assert A.kvq_decode_path(t4, 128, 8, 12) == -1     # block_size
+    assert A.kvq_decode_path(99, 128, 8, 16) == -1     # format
+    assert A.kvq_decode_path(t4, 128, 8, 16) in (0, 1)

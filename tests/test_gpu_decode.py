@@ -198,3 +198,15 @@ def test_decode_graph_replay():
         torch.cuda.synchronize()
         assert_decode_close(out.cpu().numpy().astype(np.float64), oracle_decode(case))
         assert int(torch.count_nonzero(ws)) == 0
+
+
+def test_decode_path_on_gb300():
+    """The TMA-staged kernel serves the BF16/FP8/Turbo4/NVFP4 K sides at head
+    dim 64/128 (unless KVQ_DECODE_KERNEL=mma forces the cp.async kernel, as
+    this module's second pass does); the cp.async kernel serves the rest."""
+    import os
+    tma = os.environ.get("KVQ_DECODE_KERNEL", "") != "mma"
+    assert ops.decode_kernel("turbo4", 128, 8, 16) == ("decode_tma_kernel" if tma else "decode_tc_kernel")
+    assert ops.decode_kernel("bf16k_turbo3v", 128, 8, 16) == ("decode_tma_kernel" if tma else "decode_tc_kernel")
+    assert ops.decode_kernel("turbo8", 128, 8, 16) == "decode_tc_kernel"
+    assert ops.decode_kernel("turbo4", 256, 8, 16) == "decode_tc_kernel"
