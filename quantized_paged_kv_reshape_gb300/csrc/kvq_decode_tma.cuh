@@ -956,22 +956,34 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       if (tid == 0) st[5] = sa + nsl;
       const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
       dirty = true;   // the merge of the previous unit wrote over the rings
+      // query row j of the unit's sequence (rows >= rep zero)
+      auto q_row = [&](int j, float (&xq)[E]) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) xq[i] = 0.f;
+        if (j < a.rep) {
+          const int64_t qoff = (int64_t)sq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
+#pragma unroll
+          for (int i = 0; i < E; ++i)
+            xq[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
+                             : reinterpret_cast<const float*>(a.q)[qoff + i];
+        }
+      };
+      // a warp's first query row is requested before the copies go out: behind
+      // them in the memory queues it would wait for their bytes
+      float xq0[E];
+      if (first_stretch && warp < 8) q_row(warp, xq0);
       for (int s = 0; s < NST && s < my; ++s) issue(s, (gk + (uint32_t)s) % NST);
       if (first_stretch) {
         // ---- queries (rotated when K is stored rotated), rows >= rep zero
         for (int j = warp; j < 8; j += NW) {
           float xq[E];
-          if (j < a.rep) {
-            const int64_t qoff = (int64_t)sq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
+          if (j == warp) {
 #pragma unroll
-            for (int i = 0; i < E; ++i)
-              xq[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
-                               : reinterpret_cast<const float*>(a.q)[qoff + i];
-            if constexpr (side_rotated(KS)) fwht_warp<E>(xq, lane, a.inv_sqrt_hd);
+            for (int i = 0; i < E; ++i) xq[i] = xq0[i];
           } else {
-#pragma unroll
-            for (int i = 0; i < E; ++i) xq[i] = 0.f;
+            q_row(j, xq);
           }
+          if constexpr (side_rotated(KS)) fwht_warp<E>(xq, lane, a.inv_sqrt_hd);
 #pragma unroll
           for (int i = 0; i < E; ++i) q_s[j * HD + lane * E + i] = xq[i];
         }
