@@ -510,7 +510,8 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
   // stage (gk + s) % NST (lane 0).  Pieces of 16 rows (block_size >= 16) or
   // two of 8 (block_size 8); a piece outside the attended range or whose
   // block id is invalid is not copied.
-  bool dirty = true;      // a stage holds generic-proxy writes the copies must follow
+  bool dirty = false;     // a stage holds generic-proxy writes the copies must follow
+  bool merged = false;    // a unit's merge has run in this CTA (it overlaps the rings)
   auto issue = [&](int s, uint32_t st) {
     // Every lane computes the same operands (the block ids are broadcast
     // from lane 0), so that the copies' operands are warp-uniform; lane 0
@@ -955,7 +956,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       __syncthreads();
       if (tid == 0) st[5] = sa + nsl;
       const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
-      dirty = true;   // the merge of the previous unit wrote over the rings
+      if (first_stretch && merged) dirty = true;   // the previous unit's merge wrote over the rings
       // query row j of the unit's sequence (rows >= rep zero)
       auto q_row = [&](int j, float (&xq)[E]) {
 #pragma unroll
@@ -1100,6 +1101,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       gk += (uint32_t)my;
     }
 
+    merged = true;
     // ---- merge of the unit's warps (as decode_tc_kernel)
     const int64_t x = st[0], off_u = st[4];
     const int seq_u = (int)st[2], kvh_u = kvh;
@@ -1206,21 +1208,38 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       if (*last_s) {
         __threadfence();
         for (int r = warp; r < a.rep; r += NW) {
+          // one pass over the partials, four loaded at a time, with the
+          // running maximum rescaling what is summed so far
           const float* pr = part0 + (int64_t)r * a.kmax * (HD + 4);
-          float mm = -CUDART_INF_F;
-          for (int i = 0; i < np; ++i) mm = fmaxf(mm, __ldcg(pr + i * (HD + 4)));
+          float mm = -CUDART_INF_F, ll = 0.f;
           float xr[E];
 #pragma unroll
           for (int e = 0; e < E; ++e) xr[e] = 0.f;
-          float ll = 0.f;
-          if (mm != -CUDART_INF_F) {
-            for (int i = 0; i < np; ++i) {
-              const float* pi = pr + i * (HD + 4);
-              const float mi_ = __ldcg(pi);
-              const float w = mi_ == -CUDART_INF_F ? 0.f : exp2f(mi_ - mm);
-              ll = fmaf(__ldcg(pi + 1), w, ll);
+          for (int i0 = 0; i0 < np; i0 += 4) {
+            float mi[4], li[4], xi[4][E];
 #pragma unroll
-              for (int e = 0; e < E; ++e) xr[e] = fmaf(__ldcg(pi + 4 + lane * E + e), w, xr[e]);
+            for (int u = 0; u < 4; ++u) {
+              const float* pi = pr + (i0 + u) * (HD + 4);
+              const bool in = i0 + u < np;
+              mi[u] = in ? __ldcg(pi) : -CUDART_INF_F;
+              li[u] = in ? __ldcg(pi + 1) : 0.f;
+#pragma unroll
+              for (int e = 0; e < E; ++e) xi[u][e] = in ? __ldcg(pi + 4 + lane * E + e) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (mi[u] == -CUDART_INF_F) continue;
+              if (mi[u] > mm) {
+                const float sc = mm == -CUDART_INF_F ? 0.f : exp2f(mm - mi[u]);
+                ll *= sc;
+#pragma unroll
+                for (int e = 0; e < E; ++e) xr[e] *= sc;
+                mm = mi[u];
+              }
+              const float w = exp2f(mi[u] - mm);
+              ll = fmaf(li[u], w, ll);
+#pragma unroll
+              for (int e = 0; e < E; ++e) xr[e] = fmaf(xi[u][e], w, xr[e]);
             }
           }
           finish_row(r, xr, ll);
