@@ -255,7 +255,7 @@ struct TmCfg {
   // pair / quad tables: entry of index b at b * 256; K's in bytes [0, 128)
   // of an entry, V's in [128, 256) unless it is K's table
   static constexpr bool VLUT2 = V::CB && !(K::CB && KS == VS);
-  static constexpr int MAXP = 512;                        // pages staged per stretch
+  static constexpr int MAXP = 2048;                       // pages staged per stretch
   static constexpr int OFF_Q = 0;                         // q rows [8][HD] fp32
   static constexpr int OFF_BLK = OFF_Q + 8 * HD * 4;      // block ids of a stretch
   static constexpr int OFF_SCAN = OFF_BLK + MAXP * 4;     // partition scan / merge scratch
