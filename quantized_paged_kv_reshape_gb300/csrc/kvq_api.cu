@@ -123,28 +123,6 @@ const Codebooks& codebooks() {
     fill(4, g_cb.lv4, g_cb.th4);
     fill(3, g_cb.lv3, g_cb.th3);
     fill(2, g_cb.lv2, g_cb.th2);
-    // Codebook-search buckets (kvq_common.cuh, lm_code_bucket): bucket k
-    // covers the magnitudes whose fp32 bits >> 20 equal kBucketLo + k (the
-    // ends absorb everything below / above); base = positive thresholds
-    // below the bucket, thr = the bucket's positive threshold (at most one).
-    auto buckets = [](const float* th, int n, uint32_t (*out)[2]) {
-      for (int k = 0; k < kBuckets; ++k) {
-        uint32_t lo_bits = k == 0 ? 0u : (uint32_t)(kBucketLo + k) << 20;
-        uint32_t hi_bits = k == kBuckets - 1 ? 0x7f800001u : (uint32_t)(kBucketLo + k + 1) << 20;
-        uint32_t base = 0, thr = 0x7fffffffu;
-        int inside = 0;
-        for (int i = 0; i < n; ++i) {
-          if (!(th[i] > 0.f)) continue;
-          uint32_t tb;
-          std::memcpy(&tb, &th[i], 4);
-          if (tb < lo_bits) ++base;
-          else if (tb < hi_bits) { thr = tb; ++inside; }
-        }
-        if (inside > 1) std::abort();  // bucket wider than the threshold spacing
-        out[k][0] = base;
-        out[k][1] = thr;
-      }
-    };
     // The cache write's Turbo4/3 search buckets quotients by fmaf(v, 4, 2^20 +
     // 128.5) rounded to eighths: edges (k - 128.5) / 4 blur by up to 1/64, so
     // no threshold may lie that close to one.
@@ -157,9 +135,6 @@ const Codebooks& codebooks() {
     };
     check_edges(g_cb.th4, 15);
     check_edges(g_cb.th3, 7);
-    buckets(g_cb.th4, 15, g_cb.bucket[0]);
-    buckets(g_cb.th3, 7, g_cb.bucket[1]);
-    buckets(g_cb.th2, 3, g_cb.bucket[2]);
     static const float e2m1_mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
     for (int c2 = 0; c2 < 16; ++c2) g_cb.e2m1[c2] = (c2 & 8) ? -e2m1_mag[c2 & 7] : e2m1_mag[c2 & 7];
   });

@@ -21,14 +21,6 @@ enum Side : int { S_BF16 = 0, S_FP8 = 1, S_NVFP4 = 2, S_T4 = 3, S_T3 = 4, S_T2 =
 
 constexpr int kGroup = 16;  // one scale per 16 consecutive elements
 
-// Codebook-search buckets: bucket k of a magnitude m >= 0 with fp32 bits mb
-// is clamp(mb >> 20, kBucketLo, kBucketLo + kBuckets - 1) - kBucketLo, i.e.
-// the exponent and top 3 mantissa bits; bucket 0 holds [0, 0.140625), the
-// last one [4, inf).  Every bucket is narrower than the spacing of the
-// positive Lloyd-Max thresholds (>= 0.258), so it holds at most one.
-constexpr int kBucketLo = 992;  // bits(0.125f) >> 20
-constexpr int kBuckets = 41;    // up to bits(4.0f) >> 20 = 1032
-
 // Stored bits per element in the code / raw-data section.
 __host__ __device__ constexpr int side_bits(int s) {
   return s == S_BF16 ? 16 : s == S_FP8 ? 8 : s == S_T4 ? 4 : s == S_T3 ? 3
@@ -59,24 +51,7 @@ struct Codebooks {
   float lv3[8], th3[7];
   float lv2[4], th2[3];
   float e2m1[16];
-  // Bucket tables of the codebook search (see lm_code_bucket), for 4, 3
-  // and 2 bits: per bucket (number of positive thresholds below the
-  // bucket, bit pattern of the bucket's one positive threshold or
-  // 0x7fffffff for none).
-  uint32_t bucket[3][kBuckets][2];
 };
-
-// E2M1 code of v: round to nearest, ties to the even code, saturating at 6,
-// sign bit 3 given by the caller.  The magnitude code counts the midpoints
-// below |v|; a midpoint itself goes up only where the code above is even.
-// neg: the sign bit to store (that of the unrounded quotient).
-__device__ __forceinline__ uint32_t e2m1_from_float(float v, bool neg) {
-  const float m = fabsf(v);
-  const uint32_t c = (uint32_t)(m > 0.25f) + (uint32_t)(m >= 0.75f) + (uint32_t)(m > 1.25f) +
-                     (uint32_t)(m >= 1.75f) + (uint32_t)(m > 2.5f) + (uint32_t)(m >= 3.5f) +
-                     (uint32_t)(m > 5.0f);
-  return c | (neg ? 8u : 0u);
-}
 
 // ------------------------------------------------------- number formats
 
@@ -139,26 +114,6 @@ __device__ __forceinline__ void fwht_warp(float (&x)[E], int lane, float inv_sqr
 }
 
 // ---------------------------------------------------- codebook search
-
-// code = number of thresholds <= v for a symmetric 2^B-level codebook (the
-// middle threshold is 0, the others come in pairs +-t), from the bucket
-// table of the positive thresholds:
-//   v >= 0 (and -0): code = 2^(B-1)     + #{t > 0 : t <= v}
-//   v <  0         : code = 2^(B-1) - 1 - #{t > 0 : t <  |v|}
-// The count is the bucket's base count plus one compare of |v| with the
-// bucket's threshold (on the bit patterns, which order like the values for
-// non-negative floats; "<" becomes ">=" against the next pattern).
-template <int B>
-__device__ __forceinline__ int lm_code_bucket(float v, const uint2* table) {
-  const uint32_t vb = __float_as_uint(v + 0.0f);  // -0 becomes +0
-  const uint32_t neg = vb >> 31;
-  const uint32_t mb = vb & 0x7fffffffu;
-  const uint32_t k = min(max(mb >> 20, (uint32_t)kBucketLo), (uint32_t)(kBucketLo + kBuckets - 1)) -
-                     (uint32_t)kBucketLo;
-  const uint2 e = table[k];
-  const int c = (int)e.x + (mb >= e.y + neg ? 1 : 0);
-  return neg ? (1 << (B - 1)) - 1 - c : (1 << (B - 1)) + c;
-}
 
 // 2-bit codes: three thresholds, searched directly (cheaper than a table
 // lookup): code = #{i : t[i] <= v}.

@@ -76,15 +76,13 @@ __device__ float2 lin_entry(int s, int k, const Codebooks& cb) {
   return make_float2(t, __uint_as_float(c));
 }
 
-// Key-table entry of key k (NVFP4): every quotient v whose fp32 bits b
+// NVFP4 key-table entry of key k: every quotient v whose fp32 bits b
 // satisfy b >> 20 == k has code  b >= e.x ? hi : lo.  e.y holds the bytes
 // (lo, hi, lo << 4, hi << 4), the last two for codes that land in a byte's
 // upper nibble.  E2M1 rounds to nearest, ties to the even code, saturating at
 // 6: the magnitude code counts the rounding points at or below |v| (a tie
 // rounds up where the upper code is even), the sign bit is v's.
-__device__ uint2 code_entry(int s, uint32_t k, const Codebooks& cb) {
-  (void)s;
-  (void)cb;
+__device__ uint2 nvfp4_entry(uint32_t k) {
   const uint32_t neg = k >> 11, mk = k & 0x7ffu;
   // first bit patterns above 0.25, at 0.75, above 1.25, at 1.75, above 2.5,
   // at 3.5, above 5 (ties at 0.25, 1.25, 2.5, 5 stay on the even code)
@@ -585,8 +583,8 @@ cache_write_kernel(const WriteArgs a, const Codebooks cb) {
   uint2* tab_k = tabs;
   uint2* tab_v = (tk && !shared_tab) ? tabs + kKeys : tabs;
   for (int k = threadIdx.x; k < kKeys; k += kThreads) {
-    if (tk) tab_k[k] = code_entry(a.k_side, (uint32_t)k, cb);
-    if (tv && !shared_tab) tab_v[k] = code_entry(a.v_side, (uint32_t)k, cb);
+    if (tk) tab_k[k] = nvfp4_entry((uint32_t)k);
+    if (tv && !shared_tab) tab_v[k] = nvfp4_entry((uint32_t)k);
   }
   static_assert(kLin == kThreads, "one table entry of each kind per thread");
   if (a.k_side == S_T4 || a.k_side == S_T3) lin[0][threadIdx.x] = lin_entry(a.k_side, threadIdx.x, cb);
