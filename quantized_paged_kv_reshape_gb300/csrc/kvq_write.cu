@@ -411,20 +411,26 @@ __device__ __forceinline__ void encode3(const uint64_t (&p)[8], float top, uint3
   }
 }
 
-// Turbo2: 16 two-bit codes from the three thresholds, one 32-bit word.
-__device__ __forceinline__ void encode2(const float (&y)[16], const Codebooks& cb, uint32_t sr,
+// Turbo2: 16 two-bit codes from the three thresholds, one 32-bit word; the
+// quotients two elements per instruction.
+__device__ __forceinline__ void encode2(const uint64_t (&p)[8], const Codebooks& cb, uint32_t sr,
                                         uint8_t* codes, uint8_t* scale, bool ok) {
   float s, r;
-  const uint32_t sbyte = group_scale(y, cb.lv2[3], sr, s, r);
+  const uint32_t sbyte = group_scale_pairs(p, cb.lv2[3], sr, s, r);
   float th[3];
 #pragma unroll
   for (int i = 0; i < 3; ++i) th[i] = cb.th2[i];
+  const uint64_t r2 = f2(r, r), ns2 = f2(-s, -s);
+  float v[16];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint64_t q0 = f2_mul(p[k], r2);
+    const uint64_t rem = f2_fma(q0, ns2, p[k]);
+    f2_split(f2_fma(rem, r2, q0), v[k], v[k + 8]);
+  }
   uint32_t w = 0u;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float v = div_by_scale(y[i], s, r);
-    w |= (uint32_t)lm_code2(v, th) << (2 * i);
-  }
+  for (int i = 0; i < 16; ++i) w |= (uint32_t)lm_code2(v[i], th) << (2 * i);
   if (ok) {
     st32(codes, w);
     st8(scale, sbyte);
@@ -527,12 +533,13 @@ __device__ __forceinline__ void write_group(const WriteArgs& a, const Codebooks&
       encode4(p, cb.lv4[15], lin, sr, base + g * 8, ssec + g, ok);
     } else if (fmt == S_T3) {
       encode3(p, cb.lv3[7], lin, sr, base + g * 6, ssec + g, rl, ok);
+    } else if (fmt == S_T2) {
+      encode2(p, cb, sr, base + g * 4, ssec + g, ok);
     } else {
       float y[16];
 #pragma unroll
       for (int k = 0; k < 8; ++k) f2_split(p[k], y[k], y[k + 8]);
-      if (fmt == S_T2) encode2(y, cb, sr, base + g * 4, ssec + g, ok);
-      else encode8(y, base + g * 16, ssec + g * 2, ok);
+      encode8(y, base + g * 16, ssec + g * 2, ok);
     }
   }
 }
