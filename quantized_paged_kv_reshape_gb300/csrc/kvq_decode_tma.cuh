@@ -232,13 +232,15 @@ __host__ __device__ constexpr bool tma_v_side(int s) {
 }
 
 // Placement of the stage tiles in dynamic shared memory.  The code tables
-// of the codebook sides sit at shared address kLutAddr (dynamic shared memory
-// starts at kSmemBase, after the 1 KB the driver reserves per block), so that
-// one byte permute of a code word with a per-lane register forms a table
-// entry's whole address; the tiles fill the space before the tables first,
-// largest section first, then the space after them.
+// of the codebook sides sit at a shared address that is a multiple of 64 KB
+// (dynamic shared memory starts at kSmemBase, after the 1 KB the driver
+// reserves per block), so that one byte permute of a code word with a
+// per-lane register forms a table entry's whole address: 0x20000 for tables
+// of 256 entries (64 KB), 0x30000 for the 64-entry Turbo3 pair table when it
+// is the only one, which leaves one larger region below it; the tiles fill
+// the space before the tables first, largest section first, then the space
+// after them.
 constexpr int kSmemBase = 0x400;
-constexpr int kLutAddr = 0x20000;
 constexpr int kSmemLimit = 227 * 1024;
 
 struct TmLayout {
@@ -262,8 +264,11 @@ struct TmCfg {
   static constexpr int OFF_STATE = OFF_SCAN + 48 * 8;     // CTA loop state
   static constexpr int OFF_BAR = OFF_STATE + 8 * 8;       // stage barriers (<= 16 x 4)
   static constexpr int HEAD = align_up(OFF_BAR + 64 * 8, 1024);
-  static constexpr int LUT_OFF = LUT ? kLutAddr - kSmemBase : 0;   // from the dynamic base
-  static constexpr int LUT_END = LUT ? LUT_OFF + 0x10000 : 0;
+  // table entries: 64 Turbo3 pair entries when V's is the only table, else 256
+  static constexpr int LUT_ENTRIES = (!K::CB && VS == S_T3) ? 64 : 256;
+  static constexpr int LUT_ADDR = LUT_ENTRIES == 64 ? 0x30000 : 0x20000;
+  static constexpr int LUT_OFF = LUT ? LUT_ADDR - kSmemBase : 0;   // from the dynamic base
+  static constexpr int LUT_END = LUT ? LUT_OFF + LUT_ENTRIES * 256 : 0;
   static constexpr int MERGE_BYTES = 16 * 8 * HD * 4 + 16 * 8 * 2 * 4;   // (for 16 warps)
 
   // CTAs per SM (measured on GB300, llama8b layer): FP8 runs two CTAs of 8
@@ -303,7 +308,8 @@ struct TmCfg {
     return TmLayout{off[0], off[1], off[2], off[3], mg, end, end <= LIMIT};
   }
   static constexpr int pick_nw() {
-    return CPS == 1 ? (layout(16, 3).ok ? 16 : 8) : (layout(8, 3).ok ? 8 : 4);
+    return CPS == 1 ? (layout(16, 3).ok ? 16 : layout(12, 3).ok ? 12 : 8)
+                    : (layout(8, 3).ok ? 8 : 4);
   }
   static constexpr int NW = pick_nw();
   static constexpr int pick_nst() {
@@ -357,7 +363,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
   float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
   int* blk_s = reinterpret_cast<int*>(smem + C::OFF_BLK);
   int64_t* scan_s = reinterpret_cast<int64_t*>(smem + C::OFF_SCAN);
-  const uint32_t lut_k = kLutAddr;
+  const uint32_t lut_k = C::LUT_ADDR;
   const uint32_t lut_v = lut_k + (C::VLUT2 ? 128 : 0);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -477,7 +483,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       }
     } else {
       const int cbits = side == S_T3 ? 3 : 4;
-      for (int e = tid; e < 256 * 16; e += NT) {
+      for (int e = tid; e < (1 << (2 * cbits)) * 16; e += NT) {   // entries the codes index
         const int b = e >> 4, cp = e & 15;
         const float c0 = lv[b & ((1 << cbits) - 1)];
         const float c1 = lv[(b >> cbits) & ((1 << cbits) - 1)];
@@ -568,8 +574,8 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
   // table-entry address = the code byte in bits 8-15 of one of these (a
   // byte permute): the tables' base (bits 16+), this lane's copy (bits 0-6),
   // V's table half (bit 7)
-  const uint32_t laneoff8 = (uint32_t)kLutAddr | ((uint32_t)(lane & 15) << 3);
-  const uint32_t laneoff16 = (uint32_t)kLutAddr | ((uint32_t)(lane & 7) << 4);
+  const uint32_t laneoff8 = (uint32_t)C::LUT_ADDR | ((uint32_t)(lane & 15) << 3);
+  const uint32_t laneoff16 = (uint32_t)C::LUT_ADDR | ((uint32_t)(lane & 7) << 4);
   const uint32_t vlane8 = laneoff8 | (C::VLUT2 ? 0x80u : 0u);
   const uint32_t vlane16 = laneoff16 | (C::VLUT2 ? 0x80u : 0u);
   // K scale span: this head's scale bytes inside a staged scale row
