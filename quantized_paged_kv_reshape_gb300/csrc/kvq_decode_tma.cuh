@@ -519,9 +519,8 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
   bool dirty = false;     // a stage holds generic-proxy writes the copies must follow
   bool merged = false;    // a unit's merge has run in this CTA (it overlaps the rings)
   auto issue = [&](int s, uint32_t st) {
-    // Every lane computes the same operands (the block ids are broadcast
-    // from lane 0), so that the copies' operands are warp-uniform; lane 0
-    // issues.
+    // Every lane computes the same operands (all lanes read the same block
+    // ids), so that the copies' operands are warp-uniform; lane 0 issues.
     const uint32_t bar = bar0 + st * 8;
     const int slab_pos = tok0 + (warp + NW * s) * SLAB;
     int b0 = -1, b1 = -1;
@@ -531,8 +530,6 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       if (slab_pos + 8 > lo) b0 = blk_s[(slab_pos >> lbs) - p0];
       if (slab_pos + 8 < tok_end) b1 = blk_s[((slab_pos + 8) >> lbs) - p0];
     }
-    b0 = __shfl_sync(0xffffffffu, b0, 0);
-    b1 = __shfl_sync(0xffffffffu, b1, 0);
     const int rows = bs < 16 ? 8 : 16;
     const uint32_t bytes = (uint32_t)(((b0 >= 0) + (b1 >= 0)) * rows * C::ROWBYTES);
     const int in_page = slab_pos & (bs - 1);
@@ -685,26 +682,60 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       }
       const uint32_t selb = (uint32_t)(2 * (c & 1));
       const uint32_t sel0 = 0x7604u | (selb << 4), sel1 = 0x7604u | ((selb + 1) << 4);
+      if constexpr (PK) {
+        // One MMA per token row of the fragment: A's row g holds the token's
+        // hi parts, row g + 8 its lo parts, so that each table entry (hi, lo)
+        // is an operand register pair as loaded.  Output rows g / g + 8 are
+        // the hi / lo dot products, summed after the scaling.
+        float sgh[4] = {0.f, 0.f, 0.f, 0.f};   // token g: (hi, lo) rows x columns 2c, 2c+1
+        float sbh[4] = {0.f, 0.f, 0.f, 0.f};   // token g + 8
 #pragma unroll
-      for (int j = 0; j < NK; ++j) {
-        const uint32_t ka = sb + kco[j >> 1];
-        const uint32_t wa = (j & 1) ? tm::lds32o<8>(ka) : tm::lds32o<0>(ka);
-        const uint32_t wb = (j & 1) ? tm::lds32o<8 + 8 * KT::BOXW>(ka) : tm::lds32o<8 * KT::BOXW>(ka);
-        const uint2 xa0 = tm::lds64(tc::prmt(wa, laneoff8, sel0));
-        const uint2 xa1 = tm::lds64(tc::prmt(wa, laneoff8, sel1));
-        const uint2 xb0 = tm::lds64(tc::prmt(wb, laneoff8, sel0));
-        const uint2 xb1 = tm::lds64(tc::prmt(wb, laneoff8, sel1));
-        float cg[4];
-        tm::mma_z(cg, xa0.x, xb0.x, xa1.x, xb1.x, qh[j][0], qh[j][1]);
-        if constexpr (!PK) tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
-        tc::mma<false>(cg, xa0.y, xb0.y, xa1.y, xb1.y, qh[j][0], qh[j][1]);
-        const float2 gs = unpack_f16x2(tc::e4m3x2_f16x2(
-            tc::prmt(sa[j >> 2], sbw[j >> 2], (uint32_t)(j & 3) | ((uint32_t)(4 + (j & 3)) << 4))));
-        float* acc = (j & 1) ? sacl : sacc;
-        acc[0] = fmaf(cg[0], gs.x, acc[0]);
-        acc[1] = fmaf(cg[1], gs.x, acc[1]);
-        acc[2] = fmaf(cg[2], gs.y, acc[2]);
-        acc[3] = fmaf(cg[3], gs.y, acc[3]);
+        for (int j = 0; j < NK; ++j) {
+          const uint32_t ka = sb + kco[j >> 1];
+          const uint32_t wa = (j & 1) ? tm::lds32o<8>(ka) : tm::lds32o<0>(ka);
+          const uint32_t wb = (j & 1) ? tm::lds32o<8 + 8 * KT::BOXW>(ka) : tm::lds32o<8 * KT::BOXW>(ka);
+          const uint2 xa0 = tm::lds64(tc::prmt(wa, laneoff8, sel0));
+          const uint2 xa1 = tm::lds64(tc::prmt(wa, laneoff8, sel1));
+          const uint2 xb0 = tm::lds64(tc::prmt(wb, laneoff8, sel0));
+          const uint2 xb1 = tm::lds64(tc::prmt(wb, laneoff8, sel1));
+          float cg[4], cb[4];
+          tm::mma_z(cg, xa0.x, xa0.y, xa1.x, xa1.y, qh[j][0], qh[j][1]);
+          tm::mma_z(cb, xb0.x, xb0.y, xb1.x, xb1.y, qh[j][0], qh[j][1]);
+          const float2 gs = unpack_f16x2(tc::e4m3x2_f16x2(
+              tc::prmt(sa[j >> 2], sbw[j >> 2], (uint32_t)(j & 3) | ((uint32_t)(4 + (j & 3)) << 4))));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sgh[e] = fmaf(cg[e], gs.x, sgh[e]);
+            sbh[e] = fmaf(cb[e], gs.y, sbh[e]);
+          }
+        }
+        sacc[0] = sgh[0]; sacc[1] = sgh[1]; sacc[2] = sbh[0]; sacc[3] = sbh[1];
+        sacl[0] = sgh[2]; sacl[1] = sgh[3]; sacl[2] = sbh[2]; sacl[3] = sbh[3];
+      } else {
+        // q hi and lo in separate operands: rows g / g + 8 are tokens g /
+        // g + 8, the hi parts against both, the lo parts against q's hi
+        // (fewer live registers than the hi / lo rows above)
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+          const uint32_t ka = sb + kco[j >> 1];
+          const uint32_t wa = (j & 1) ? tm::lds32o<8>(ka) : tm::lds32o<0>(ka);
+          const uint32_t wb = (j & 1) ? tm::lds32o<8 + 8 * KT::BOXW>(ka) : tm::lds32o<8 * KT::BOXW>(ka);
+          const uint2 xa0 = tm::lds64(tc::prmt(wa, laneoff8, sel0));
+          const uint2 xa1 = tm::lds64(tc::prmt(wa, laneoff8, sel1));
+          const uint2 xb0 = tm::lds64(tc::prmt(wb, laneoff8, sel0));
+          const uint2 xb1 = tm::lds64(tc::prmt(wb, laneoff8, sel1));
+          float cg[4];
+          tm::mma_z(cg, xa0.x, xb0.x, xa1.x, xb1.x, qh[j][0], qh[j][1]);
+          tc::mma<false>(cg, xa0.x, xb0.x, xa1.x, xb1.x, ql[j][0], ql[j][1]);
+          tc::mma<false>(cg, xa0.y, xb0.y, xa1.y, xb1.y, qh[j][0], qh[j][1]);
+          const float2 gs = unpack_f16x2(tc::e4m3x2_f16x2(
+              tc::prmt(sa[j >> 2], sbw[j >> 2], (uint32_t)(j & 3) | ((uint32_t)(4 + (j & 3)) << 4))));
+          float* acc = (j & 1) ? sacl : sacc;
+          acc[0] = fmaf(cg[0], gs.x, acc[0]);
+          acc[1] = fmaf(cg[1], gs.x, acc[1]);
+          acc[2] = fmaf(cg[2], gs.y, acc[2]);
+          acc[3] = fmaf(cg[3], gs.y, acc[3]);
+        }
       }
     }
 #pragma unroll
@@ -953,13 +984,15 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       p0 = tok0 >> lbs;
       const int p1 = ((tok_end - 1) >> lbs) + 1;
       const int64_t tab = (int64_t)sq * a.max_blocks;
+      int bad_ids = 0;
       for (int i = tid; i < p1 - p0; i += NT) {
         const int64_t b = a.block_tables[tab + p0 + i];
         const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
         if (bad && a.err) atomicOr(a.err, 2);
+        bad_ids |= bad;
         blk_s[i] = bad ? -1 : (int)b;
       }
-      __syncthreads();
+      const bool any_bad_id = __syncthreads_or(bad_ids) != 0;   // in this stretch
       if (tid == 0) st[5] = sa + nsl;
       const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
       if (first_stretch && merged) dirty = true;   // the previous unit's merge wrote over the rings
@@ -1031,7 +1064,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
           bool ok = pos >= lo && pos < tok_end;
           if (ok) ok = blk_s[(pos >> lbs) - p0] >= 0;
           bad = __ballot_sync(0xffffffffu, !ok) & 0xffffu;
-        } else {
+        } else if (any_bad_id) {
           if (blk_s[(slab_pos >> lbs) - p0] < 0) bad = 0xffffu;
         }
         if (bad == 0xffffu) {   // nothing to attend here
