@@ -248,7 +248,7 @@ struct TmLayout {
   bool ok;
 };
 
-template <int KS, int VS, int HD>
+template <int KS, int VS, int HD, bool PK>
 struct TmCfg {
   using K = TmSide<KS, HD>;
   using V = TmSide<VS, HD>;
@@ -307,7 +307,14 @@ struct TmCfg {
     if (mg + MERGE_BYTES > end) end = mg + MERGE_BYTES;
     return TmLayout{off[0], off[1], off[2], off[3], mg, end, end <= LIMIT};
   }
+  // Warps per CTA: as many as the stage rings allow (16, 12 or 8), except
+  // that a codebook K side with unpacked queries (q hi and lo in separate
+  // operands: the most live registers) runs 12 warps of up to 168 registers
+  // (measured on GB300, long-context layer: 315 against 330 us with 16
+  // warps of 128 registers, which spill; with packed queries 16 warps are
+  // faster: 82 against 84 us).
   static constexpr int pick_nw() {
+    if (K::CB && !PK && CPS == 1 && layout(12, 3).ok) return 12;
     return CPS == 1 ? (layout(16, 3).ok ? 16 : layout(12, 3).ok ? 12 : 8)
                     : (layout(8, 3).ok ? 8 : 4);
   }
@@ -343,9 +350,9 @@ __device__ __forceinline__ int tm_v_row_dim(int i, int row) {
 }
 
 template <int KS, int VS, int HD, bool PK>
-__global__ void __launch_bounds__(32 * TmCfg<KS, VS, HD>::NW, TmCfg<KS, VS, HD>::CPS)
+__global__ void __launch_bounds__(32 * TmCfg<KS, VS, HD, PK>::NW, TmCfg<KS, VS, HD, PK>::CPS)
 decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, const Codebooks cb) {
-  using C = TmCfg<KS, VS, HD>;
+  using C = TmCfg<KS, VS, HD, PK>;
   using KT = typename C::K;
   using VT = typename C::V;
   constexpr int NW = C::NW;
@@ -1307,7 +1314,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
 template <int KS, int VS, int HD, bool PK>
 cudaError_t launch_tma_kern(const DecodeArgs& a, const TmaMaps& maps, const Codebooks& cb,
                             cudaStream_t st) {
-  using C = TmCfg<KS, VS, HD>;
+  using C = TmCfg<KS, VS, HD, PK>;
   static_assert(C::SMEM <= kSmemLimit, "shared memory budget");
   static_assert(C::NST >= 2, "at least two stages per warp");
   auto kern = decode_tma_kernel<KS, VS, HD, PK>;
