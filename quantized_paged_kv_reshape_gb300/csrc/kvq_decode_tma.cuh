@@ -307,16 +307,22 @@ struct TmCfg {
     if (mg + MERGE_BYTES > end) end = mg + MERGE_BYTES;
     return TmLayout{off[0], off[1], off[2], off[3], mg, end, end <= LIMIT};
   }
-  // Warps per CTA: as many as the stage rings allow (16, 12 or 8), except
-  // that a codebook K side with unpacked queries (q hi and lo in separate
-  // operands: the most live registers) runs 12 warps of up to 168 registers
-  // (measured on GB300, long-context layer: 315 against 330 us with 16
-  // warps of 128 registers, which spill; with packed queries 16 warps are
-  // faster: 82 against 84 us).
+  // Warps per CTA: as many as rings of three stages allow (16, 12 or 8),
+  // with these exceptions, measured on GB300:
+  // - a codebook K side with unpacked queries (q hi and lo in separate
+  //   operands: the most live registers) runs 12 warps of up to 168
+  //   registers (long-context layer: 315 against 330 us with 16 warps of 128
+  //   registers, which spill; with packed queries 16 warps are faster: 82
+  //   against 84 us);
+  // - with a code table, 12 warps of two stages beat 8 of three (BF16 K
+  //   with Turbo4 V 74.0 against 80.2 us, with Turbo2 V 70.0 against 77.8;
+  //   without a table, BF16 K and V: 91.2 against 90.6 us).
   static constexpr int pick_nw() {
     if (K::CB && !PK && CPS == 1 && layout(12, 3).ok) return 12;
-    return CPS == 1 ? (layout(16, 3).ok ? 16 : layout(12, 3).ok ? 12 : 8)
-                    : (layout(8, 3).ok ? 8 : 4);
+    if (CPS != 1) return layout(8, 3).ok ? 8 : 4;
+    if (layout(16, 3).ok) return 16;
+    if (layout(12, 3).ok || (LUT && layout(12, 2).ok)) return 12;
+    return 8;
   }
   static constexpr int NW = pick_nw();
   static constexpr int pick_nst() {
