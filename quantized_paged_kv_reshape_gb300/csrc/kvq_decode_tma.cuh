@@ -967,65 +967,87 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
   constexpr float kLazy = 8.0f;    // the running maximum trails by at most this (log2 units)
   constexpr float kNoMax = -1e30f;  // running maximum before any score (finite: exp2 of
                                     // a masked score minus it is 0, never NaN)
-  for (;;) {
-    __syncthreads();
-    {
-      const int64_t x = st[0];
-      if (x >= st[1]) break;
-      int first, n, len;
-      seq_slabs((int)st[2], first, n, lo, len);
-      if (tid == 0) {
-        st[5] = first + st[4];
-        st[6] = first + st[4] + min((int64_t)n - st[4], st[1] - x);
-      }
+  // state of the open stretch (set by open_stretch)
+  int s_sq = 0, s_nsl = 0, s_my = 0;
+  bool s_any_bad = false;
+  float xq0[E];   // this warp's first query row, requested with the unit's first copies
+  // query row j of the unit's sequence (rows >= rep zero)
+  auto q_row = [&](int j, float (&xq)[E]) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) xq[i] = 0.f;
+    if (j < a.rep) {
+      const int64_t qoff = (int64_t)s_sq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        xq[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
+                         : reinterpret_cast<const float*>(a.q)[qoff + i];
     }
+  };
+  // Unit bounds from the CTA loop state (st[0] = next slab of the range,
+  // st[2] its sequence, st[4] the slab offset in it): st[5], st[6] = the
+  // unit's first and end slab.  False when the range is done.
+  auto open_unit = [&]() -> bool {
+    const int64_t x = st[0];
+    if (x >= st[1]) return false;
+    int first, n, len;
+    seq_slabs((int)st[2], first, n, lo, len);
+    if (tid == 0) {
+      st[5] = first + st[4];
+      st[6] = first + st[4] + min((int64_t)n - st[4], st[1] - x);
+    }
+    return true;
+  };
+  // Next stretch of the unit (after a __syncthreads): its block ids into
+  // shared memory, then each warp's first copies (the first stretch of a
+  // unit also requests the warp's first query row before them: behind them
+  // in the memory queues it would wait for their bytes).  False when the
+  // unit has no slabs left.  Called by every thread.
+  auto open_stretch = [&](bool first_stretch) -> bool {
+    const int64_t sa = st[5], s_hi = st[6];
+    if (sa >= s_hi) return false;
+    s_sq = (int)st[2];
+    int first, n, len;
+    seq_slabs(s_sq, first, n, lo, len);
+    const int sub = (C::MAXP - 1) * bs / SLAB;
+    s_nsl = (int)min((int64_t)sub, s_hi - sa);
+    tok0 = (int)(sa * SLAB);
+    tok_end = min(tok0 + s_nsl * SLAB, len);
+    p0 = tok0 >> lbs;
+    const int p1 = ((tok_end - 1) >> lbs) + 1;
+    const int64_t tab = (int64_t)s_sq * a.max_blocks;
+    int bad_ids = 0;
+    for (int i = tid; i < p1 - p0; i += NT) {
+      const int64_t b = a.block_tables[tab + p0 + i];
+      const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
+      if (bad && a.err) atomicOr(a.err, 2);
+      bad_ids |= bad;
+      blk_s[i] = bad ? -1 : (int)b;
+    }
+    s_any_bad = __syncthreads_or(bad_ids) != 0;   // in this stretch
+    if (tid == 0) st[5] = sa + s_nsl;
+    s_my = s_nsl > warp ? (s_nsl - 1 - warp) / NW + 1 : 0;
+    if (first_stretch && merged) dirty = true;   // the previous unit's merge wrote over the rings
+    if (first_stretch && warp < 8) q_row(warp, xq0);
+    for (int s = 0; s < NST && s < s_my; ++s) issue(s, (gk + (uint32_t)s) % NST);
+    return true;
+  };
+  // the next unit's first stretch was opened during this unit's merge
+  bool pre_opened = false;
+  for (;;) {
+    __syncthreads();   // (a pre-opened unit: the previous merge is done with q_s)
+    if (!pre_opened && !open_unit()) break;
 #pragma unroll
     for (int i = 0; i < NK; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     m0 = m1 = kNoMax;
     l0 = l1 = 0.f;
     for (int first_stretch = 1;; first_stretch = 0) {
-      __syncthreads();
-      const int64_t sa = st[5], s_hi = st[6];
-      if (sa >= s_hi) break;
-      const int sq = (int)st[2];
-      int first, n, len;
-      seq_slabs(sq, first, n, lo, len);
-      const int sub = (C::MAXP - 1) * bs / SLAB;
-      const int nsl = (int)min((int64_t)sub, s_hi - sa);
-      tok0 = (int)(sa * SLAB);
-      tok_end = min(tok0 + nsl * SLAB, len);
-      p0 = tok0 >> lbs;
-      const int p1 = ((tok_end - 1) >> lbs) + 1;
-      const int64_t tab = (int64_t)sq * a.max_blocks;
-      int bad_ids = 0;
-      for (int i = tid; i < p1 - p0; i += NT) {
-        const int64_t b = a.block_tables[tab + p0 + i];
-        const bool bad = b < 0 || (a.num_blocks > 0 && b >= a.num_blocks);
-        if (bad && a.err) atomicOr(a.err, 2);
-        bad_ids |= bad;
-        blk_s[i] = bad ? -1 : (int)b;
+      if (!(first_stretch && pre_opened)) {
+        __syncthreads();
+        if (!open_stretch(first_stretch != 0)) break;
       }
-      const bool any_bad_id = __syncthreads_or(bad_ids) != 0;   // in this stretch
-      if (tid == 0) st[5] = sa + nsl;
-      const int my = nsl > warp ? (nsl - 1 - warp) / NW + 1 : 0;
-      if (first_stretch && merged) dirty = true;   // the previous unit's merge wrote over the rings
-      // query row j of the unit's sequence (rows >= rep zero)
-      auto q_row = [&](int j, float (&xq)[E]) {
-#pragma unroll
-        for (int i = 0; i < E; ++i) xq[i] = 0.f;
-        if (j < a.rep) {
-          const int64_t qoff = (int64_t)sq * a.q_stride + (int64_t)(kvh * a.rep + j) * HD + lane * E;
-#pragma unroll
-          for (int i = 0; i < E; ++i)
-            xq[i] = a.q_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(a.q)[qoff + i])
-                             : reinterpret_cast<const float*>(a.q)[qoff + i];
-        }
-      };
-      // a warp's first query row is requested before the copies go out: behind
-      // them in the memory queues it would wait for their bytes
-      float xq0[E];
-      if (first_stretch && warp < 8) q_row(warp, xq0);
-      for (int s = 0; s < NST && s < my; ++s) issue(s, (gk + (uint32_t)s) % NST);
+      pre_opened = false;
+      const int my = s_my;
+      const bool any_bad_id = s_any_bad;
       if (first_stretch) {
         // ---- queries (rotated when K is stored rotated), rows >= rep zero
         for (int j = warp; j < 8; j += NW) {
@@ -1218,7 +1240,31 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
         red_s[2 * r + 1] = lsum;
       }
     }
+    // The rings are free again: advance the CTA loop state and open the next
+    // unit's first stretch now, so that its first copies are in flight while
+    // this unit's partials go out (global stores, the counter's round trip
+    // and the last arriver's merge).  Measured on GB300: FP8 K 57.6 -> 57.3,
+    // long-context Turbo4 K 315.7 -> 307.8, ragged FP8 K 219.3 -> 216.6 us;
+    // with BF16 K (the largest burst of copies) the partials waited behind
+    // them (llama8b 90.6 -> 91.9 us), so BF16 K opens the unit afterwards.
+    if (tid == 0) {
+      int s2 = seq_u, n2 = 0;
+      do {
+        ++s2;
+        if (s2 >= N) break;
+        int f2, l2, e2;
+        seq_slabs(s2, f2, n2, l2, e2);
+      } while (n2 == 0);
+      st[0] = x + take;
+      st[2] = s2 < N ? s2 : N - 1;
+      st[4] = 0;
+      if (s2 >= N) st[1] = st[0];
+    }
     __syncthreads();
+    if (KS != S_BF16 && open_unit()) {
+      __syncthreads();
+      pre_opened = open_stretch(true);
+    }
     const int64_t row0 = (int64_t)seq_u * a.nq + kvh_u * a.rep;
     float* part0 = a.part + row0 * a.kmax * (HD + 4);
     auto finish_row = [&](int r, float (&xr)[E], float lsum) {
@@ -1301,19 +1347,6 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       }
     }
 
-    if (tid == 0) {
-      int s2 = seq_u, n2 = 0;
-      do {
-        ++s2;
-        if (s2 >= N) break;
-        int f2, l2, e2;
-        seq_slabs(s2, f2, n2, l2, e2);
-      } while (n2 == 0);
-      st[0] = x + take;
-      st[2] = s2 < N ? s2 : N - 1;
-      st[4] = 0;
-      if (s2 >= N) st[1] = st[0];
-    }
   }
 }
 
