@@ -270,6 +270,11 @@ struct TmCfg {
   static constexpr int LUT_OFF = LUT ? LUT_ADDR - kSmemBase : 0;   // from the dynamic base
   static constexpr int LUT_END = LUT ? LUT_OFF + LUT_ENTRIES * 256 : 0;
   static constexpr int MERGE_BYTES = 16 * 8 * HD * 4 + 16 * 8 * 2 * 4;   // (for 16 warps)
+  // Virtual slabs a unit costs in the partition (measured on GB300 with
+  // U = 0 / 24 / 48 / 96: ragged bf16k_turbo3v 264.5 / 254.4 / 244.2 /
+  // 250.4 us, fp8k_turbo2v 219.4 / 210.9 / 203.1 / 199.2, llama8b bf16 92.5 /
+  // 91.7 / 91.1 / 94.2, turbo4 82.2 / 81.2 / 79.9 / 81.9).
+  static constexpr int SWITCH = 48;
 
   // CTAs per SM (measured on GB300, llama8b layer): FP8 runs two CTAs of 8
   // warps, whose unit boundaries (merge, next unit's first copies) then
@@ -422,8 +427,9 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
     longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, d));
   }
   // scan_s: [0, 16) per-warp slab sums, [16, 32) per-warp longest rows,
-  // [32] / [33] the first unit's sequence / slab, [36, 44) merge maxima and
-  // sums (float), [44] the last-arriver flag (int)
+  // [32] / [33] the first unit's sequence / slab, [34] / [35] the range's
+  // first and end slab, [36, 44) merge maxima and sums (float), [44] the
+  // last-arriver flag (int)
   if (lane == 31) scan_s[warp] = incl;
   if (lane == 0) scan_s[16 + warp] = longest;
   __syncthreads();
@@ -435,11 +441,31 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
     max_n = max(max_n, scan_s[16 + w2]);
   }
   const int64_t excl = before + incl - mine;
-  int64_t cpc = (total + R - 1) / R;
+  // Sequence s spans [P_s + U s, P_s + U s + U + n_s) of a virtual slab line
+  // (P_s = attended slabs before it): its first U positions stand for the
+  // cost of a unit (the merge, then the first copies' round trip), and the
+  // CTAs split the virtual line evenly, so that a CTA that works on more
+  // sequences takes fewer slabs.  Real slab (s, o) sits at P_s + U (s + 1) + o.
+  constexpr int64_t U = C::SWITCH;
+  const int64_t totalv = total + U * N;
+  int64_t cpc = (totalv + R - 1) / R;
   if (a.kmax > 1) cpc = max(cpc, (max_n + a.kmax - 2) / (a.kmax - 1));
   if (cpc < 1) cpc = 1;
-  const int64_t x0 = (int64_t)jr * cpc;
-  const int64_t x_end = min(x0 + cpc, total);
+  const int64_t v0 = (int64_t)jr * cpc, v1 = min(v0 + cpc, totalv);
+  {   // the real slab indices of v0 and v1 (scan_s[34], [35])
+    int64_t P = excl;
+    for (int s = s_beg; s < s_end; ++s) {
+      int f, n, l_, e_;
+      seq_slabs(s, f, n, l_, e_);
+      const int64_t vp = P + U * s;
+      if (v0 >= vp && v0 < vp + U + n) scan_s[34] = P + min(max(v0 - vp - U, (int64_t)0), (int64_t)n);
+      if (v1 >= vp && v1 < vp + U + n) scan_s[35] = P + min(max(v1 - vp - U, (int64_t)0), (int64_t)n);
+      P += n;
+    }
+  }
+  __syncthreads();
+  const int64_t x0 = v0 < totalv ? scan_s[34] : total;
+  const int64_t x_end = v1 < totalv ? scan_s[35] : total;
   if (blockIdx.x == 0) {  // sequences with nothing to attend get zero rows
     for (int s = s_beg; s < s_end; ++s) {
       int f, n, l_, e_;
@@ -1183,8 +1209,9 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
     seq_slabs(seq_u, first_u, n_u, lo_u, len_u);
     const int64_t take = min((int64_t)n_u - off_u, st[1] - x);
     const int64_t ou = x - off_u, cp = st[7];
-    const int slot = (int)(jr - ou / cp);
-    const int np = (int)((ou + n_u - 1) / cp - ou / cp + 1);
+    const int64_t vu = ou + C::SWITCH * (int64_t)(seq_u + 1);   // the row's first slab on the virtual line
+    const int slot = (int)(jr - vu / cp);
+    const int np = (int)((vu + n_u - 1) / cp - vu / cp + 1);
 #pragma unroll
     for (int msk = 4; msk < 32; msk <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
