@@ -216,7 +216,15 @@ struct T5Cfg {
   static constexpr int OFF_PV = OFF_PK + (SHARE_PAIRS ? 0 : pair_entries<KS>() * 8);
   static constexpr int OFF_MX = OFF_PV + pair_entries<VS>() * 8;  // [NSPLIT][ROWS] part-row maxima / sums
   static constexpr int OFF_BAR = OFF_MX + NSPLIT * ROWS * 4;  // 2 mbarriers, tensor-memory address
-  static constexpr int SMEM_MAIN = OFF_BAR + 32;
+  // Block ids of the tile's first BLKC pages staged in shared memory at the
+  // start (measured on GB300, 8 x 4096 with 512-token chunks: Turbo4 1359 ->
+  // 1335 us, head_dim 256 BF16 / Turbo2 / Turbo8 4142 / 5958 / 5668 -> 4047 /
+  // 5866 / 5628 us); BF16 and FP8 K at head_dim 64/128 load them at the
+  // copies' issue (staged: 896 -> 903 and 893 -> 903 us).
+  static constexpr int BLKC = (HD == 256 || side_codebook(KS)) ? 1024 : 0;
+  static_assert(BLKC % NT == 0, "block ids per thread");
+  static constexpr int OFF_BLKC = OFF_BAR + 32;
+  static constexpr int SMEM_MAIN = OFF_BLKC + BLKC * 4;
   static constexpr int OUTB = ROWS * (HD + 4) * 4;    // output staging (fp32), reuses the planes
   static constexpr int SMEM = SMEM_MAIN > OUTB ? SMEM_MAIN : OUTB;
   static constexpr int S_COL = 0, O_COL = TOK;         // tensor-memory columns of S and O
@@ -262,6 +270,22 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
   const int p_last = pbase + nq_tile - 1;
   const int lbs = 31 - __clz(a.bs);
   const int64_t tab = (int64_t)seq * a.max_blocks;
+  // steps of the tile's attended positions, and the block ids of its first
+  // BLKC pages, requested now (they are staged in shared memory after the
+  // queries, before the first copies; -1 where the table holds no valid id)
+  const int p_first = max(pbase, 0);
+  const int lo_first = a.window > 0 ? max(0, p_first + 1 - a.window) : 0;
+  const int st_begin = lo_first / TOK;
+  const int st_end = p_last >= 0 ? p_last / TOK + 1 : st_begin;
+  const int pg0 = (st_begin * TOK) >> lbs;
+  const int npg = st_end > st_begin ? min(((st_end * TOK - 1) >> lbs) + 1 - pg0, C::BLKC) : 0;
+  constexpr int BPT = C::BLKC / NT;
+  int64_t bq[BPT > 0 ? BPT : 1];
+#pragma unroll
+  for (int k = 0; k < BPT; ++k) {
+    const int i = tid + k * NT, pg = pg0 + i;
+    bq[k] = (i < npg && pg < a.max_blocks) ? a.block_tables[tab + pg] : -1;
+  }
 
   // ---- tensor memory and mbarriers
   const uint32_t bar_s = t5::smem_addr(bars), bar_o = t5::smem_addr(bars + 1);
@@ -310,19 +334,21 @@ prefill_tc5_kernel(const PrefillArgs a, const Codebooks cb) {
   t5_fill_pairs<KS>(reinterpret_cast<uint2*>(smem + C::OFF_PK), cb, tid, NT);
   if constexpr (!C::SHARE_PAIRS) t5_fill_pairs<VS>(reinterpret_cast<uint2*>(smem + C::OFF_PV), cb, tid, NT);
 
-  const int p_first = max(pbase, 0);
-  const int lo_first = a.window > 0 ? max(0, p_first + 1 - a.window) : 0;
-  const int st_begin = lo_first / TOK;
-  const int st_end = p_last >= 0 ? p_last / TOK + 1 : st_begin;
-
   // ---- raw rows of step st (positions TOK st .. TOK st + TOK - 1) into buffer b
+  int* blkc = reinterpret_cast<int*>(smem + C::OFF_BLKC);
+#pragma unroll
+  for (int k = 0; k < BPT; ++k) {
+    const int i = tid + k * NT;
+    if (i < npg) blkc[i] = (bq[k] < 0 || bq[k] > 0x7fffffff) ? -1 : (int)bq[k];
+  }
   // Block id of this thread's row of step st (-1: no row there).  With the
-  // short steps of head_dim 256 it is loaded at the top of the step that
-  // issues the copies (its latency hidden behind the step: 1-3% faster);
-  // with 64-position steps that was 8% slower than loading it at the issue.
+  // short steps of head_dim 256 it is read at the top of the step that
+  // issues the copies.
   auto row_block = [&](int st) -> int64_t {
     const int pos = st * TOK + tid / (NT / TOK);
     if (st >= st_end || pos < 0 || pos >= len) return -1;
+    const int i = (pos >> lbs) - pg0;
+    if (C::BLKC > 0 && i < C::BLKC) return blkc[i];
     return a.block_tables[tab + (pos >> lbs)];
   };
   // Thread (row t = tid / PARTS, part = tid % PARTS) looks the row's block
