@@ -1270,10 +1270,11 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
     // The rings are free again: advance the CTA loop state and open the next
     // unit's first stretch now, so that its first copies are in flight while
     // this unit's partials go out (global stores, the counter's round trip
-    // and the last arriver's merge).  Measured on GB300: FP8 K 57.6 -> 57.3,
-    // long-context Turbo4 K 315.7 -> 307.8, ragged FP8 K 219.3 -> 216.6 us;
-    // with BF16 K (the largest burst of copies) the partials waited behind
-    // them (llama8b 90.6 -> 91.9 us), so BF16 K opens the unit afterwards.
+    // and the last arriver's merge).  Measured on GB300: long-context Turbo4
+    // K 315.7 -> 307.8, ragged FP8 K with Turbo2 V 219.3 -> 216.6 us; with
+    // BF16 K (the largest burst of copies) the partials waited behind them
+    // (llama8b 90.6 -> 91.9 us), and FP8 K and V (two CTAs per SM) measured
+    // 57.4 against 56.5 us without it, so those open the unit afterwards.
     if (tid == 0) {
       int s2 = seq_u, n2 = 0;
       do {
@@ -1288,7 +1289,7 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
       if (s2 >= N) st[1] = st[0];
     }
     __syncthreads();
-    if (KS != S_BF16 && open_unit()) {
+    if (KS != S_BF16 && !(KS == S_FP8 && !C::LUT) && open_unit()) {
       __syncthreads();
       pre_opened = open_stretch(true);
     }
