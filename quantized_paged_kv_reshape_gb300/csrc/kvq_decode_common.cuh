@@ -18,6 +18,10 @@ struct SideGeom {
 };
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// Virtual slabs that stand for the cost of one unit (a merge, then the first
+// copies' round trip) in the decode kernels' work partition.
+constexpr int kUnitSlabs = 48;
 constexpr int clampi(int x, int lo, int hi) { return x < lo ? lo : x > hi ? hi : x; }
 
 template <int N>

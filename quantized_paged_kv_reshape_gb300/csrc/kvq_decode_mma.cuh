@@ -396,15 +396,37 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     max_n = max(max_n, scan_s[8 + w2]);
   }
   const int64_t excl = before + incl - mine;  // slabs before this thread's chunk
-  // Slabs per CTA: an equal share, but never so few that a row of max_n
-  // slabs spans more than kmax CTAs (the partial slots the host sized):
-  // a row of n slabs spans at most floor((n - 1) / cpc) + 2 CTAs.
-  int64_t cpc = (total + R - 1) / R;
+  // Slabs per CTA: an equal share of a virtual line on which each sequence
+  // is preceded by U slabs standing for the cost of a unit (sequence s spans
+  // [P_s + U s, P_s + U s + U + n_s), P_s = attended slabs before it), so
+  // that a CTA that works on more sequences takes fewer slabs; never so few
+  // that a row of max_n slabs spans more than kmax CTAs (the partial slots
+  // the host sized): a row of n slabs spans at most floor((n - 1) / cpc) + 2
+  // CTAs.  U = kUnitSlabs for the K sides without a code table; a codebook K
+  // side's slabs take several times longer here, so a unit costs few of them
+  // and U = 0 (measured on GB300, 16 x 8192, head_dim 256: Turbo8 259 ->
+  // 255 us with U = 48, Turbo2 288 -> 303 us).
+  constexpr int64_t U = side_codebook(KS) ? 0 : kUnitSlabs;
+  const int64_t totalv = total + U * N;
+  int64_t cpc = (totalv + R - 1) / R;
   if (a.kmax > 1) cpc = max(cpc, (max_n + a.kmax - 2) / (a.kmax - 1));
   if (cpc < 1) cpc = 1;
-  const int64_t x0 = (int64_t)jr * cpc;
-  const int64_t x_end = min(x0 + cpc, total);
+  const int64_t v0 = (int64_t)jr * cpc, v1 = min(v0 + cpc, totalv);
   __syncthreads();  // scan_s is reused below
+  {   // the real slab indices of v0 and v1 (scan_s[2], [3])
+    int64_t P = excl;
+    for (int s = s_beg; s < s_end; ++s) {
+      int f, n, l_, e_;
+      seq_slabs(s, f, n, l_, e_);
+      const int64_t vp = P + U * s;
+      if (v0 >= vp && v0 < vp + U + n) scan_s[2] = P + min(max(v0 - vp - U, (int64_t)0), (int64_t)n);
+      if (v1 >= vp && v1 < vp + U + n) scan_s[3] = P + min(max(v1 - vp - U, (int64_t)0), (int64_t)n);
+      P += n;
+    }
+  }
+  __syncthreads();
+  const int64_t x0 = v0 < totalv ? scan_s[2] : total;
+  const int64_t x_end = v1 < totalv ? scan_s[3] : total;
   if (blockIdx.x == 0) {  // sequences with nothing to attend get zero rows
     for (int s = s_beg; s < s_end; ++s) {
       int f, n, l_, e_;
@@ -1004,8 +1026,9 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     seq_slabs(seq_u, first_u, n_u, lo_u, len_u);
     const int64_t take = min((int64_t)n_u - off_u, st[1] - x);
     const int64_t ou = x - off_u, cp = st[7];                  // the unit's first slab
-    const int slot = (int)(jr - ou / cp);                      // this CTA's partial
-    const int np = (int)((ou + n_u - 1) / cp - ou / cp + 1);   // CTAs on the unit
+    const int64_t vu = ou + U * (int64_t)(seq_u + 1);         // ... on the virtual line
+    const int slot = (int)(jr - vu / cp);                      // this CTA's partial
+    const int np = (int)((vu + n_u - 1) / cp - vu / cp + 1);   // CTAs on the unit
 #pragma unroll
     for (int msk = 4; msk < 32; msk <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
