@@ -97,6 +97,26 @@ def test_decode_long_sequence_many_splits():
     assert_decode_close(gpu_decode(c), oracle_decode(c))
 
 
+@pytest.mark.parametrize("fmt,nq", [("bf16", 8), ("fp8", 8), ("turbo4", 8), ("bf16k_turbo3v", 8),
+                                    ("fp8k_turbo2v", 8), ("turbo4k_turbo3v", 16), ("turbo8", 8)])
+def test_decode_mixed_lengths(fmt, nq):
+    """Two long rows among ~100 empty or short ones: the work partition charges
+    each sequence a unit's cost, so CTAs over the short rows take few slabs
+    (some only the cost, no slab), while the long rows span several CTAs whose
+    merges take every path: the first CTA's merge from its own shared memory
+    when the others are in, the last arriver's otherwise, and the next unit
+    opened during a merge.  Run twice on one workspace, which stays zero."""
+    lens = [1] * 30 + [4100] + [0] * 3 + [17] * 40 + [2900] + [5, 16, 33] * 10
+    c = decode_case(fmt, lens, nq, 2, 128, seed=77)
+    ref = oracle_decode(c)
+    need = ops.decode_workspace_bytes(len(c["lens"]), c["nq"], c["nkv"], c["hd"], c["bs"],
+                                      c["tables"].shape[1], 0, c["fmt"])
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        assert_decode_close(gpu_decode(c, workspace=ws), ref)
+        assert int(torch.count_nonzero(ws)) == 0
+
+
 def test_sparse_v_reported():
     """Sparse-V is approximate and not parity-gated: the kernel drops weights
     <= 1e-3 of their split's running sum (never more than the oracle, which
