@@ -273,8 +273,9 @@ struct TmCfg {
   // Virtual slabs a unit costs in the partition (measured on GB300 with
   // U = 0 / 24 / 48 / 96: ragged bf16k_turbo3v 264.5 / 254.4 / 244.2 /
   // 250.4 us, fp8k_turbo2v 219.4 / 210.9 / 203.1 / 199.2, llama8b bf16 92.5 /
-  // 91.7 / 91.1 / 94.2, turbo4 82.2 / 81.2 / 79.9 / 81.9).
-  static constexpr int SWITCH = kUnitSlabs;
+  // 91.7 / 91.1 / 94.2, turbo4 82.2 / 81.2 / 79.9 / 81.9; fp8k_turbo2v again
+  // with U = 48 / 96 / 144: 201.0 / 197.2 / 203.6 us, so it takes 96).
+  static constexpr int SWITCH = (KS == S_FP8 && VS == S_T2) ? 2 * kUnitSlabs : kUnitSlabs;
 
   // CTAs per SM (measured on GB300, llama8b layer): FP8 runs two CTAs of 8
   // warps, whose unit boundaries (merge, next unit's first copies) then
