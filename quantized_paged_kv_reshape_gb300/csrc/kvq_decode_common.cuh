@@ -18,6 +18,13 @@ struct SideGeom {
 };
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+// A row of `bytes` in `chunk`-byte pieces (none when bytes is 0): do its
+// pieces divide a warp's 32 lanes evenly?
+constexpr bool chunks_split_warp(int bytes, int chunk) {
+  if (bytes == 0) return true;
+  const int n = bytes / chunk;
+  return n > 0 && 32 % n == 0;
+}
 
 // Virtual slabs that stand for the cost of one unit (a merge, then the first
 // copies' round trip) in the decode kernels' work partition.

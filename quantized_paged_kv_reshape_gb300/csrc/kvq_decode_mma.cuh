@@ -534,9 +534,8 @@ decode_tc_kernel(const DecodeArgs a, const Codebooks cb) {
     __syncwarp();  // the previous issue's reads of offs are done
     uint8_t* sb = ring + (s % C::NST) * C::STAGE;
     const int slab_pos = tok0 + (warp + NW * s) * SLAB;
-    constexpr bool FAST = (32 % (KT::ROW / KT::CH) == 0) && (32 % (VT::ROW / VT::CH) == 0) &&
-                          (KT::SROW == 0 || 32 % (KT::SROW / KT::SCH) == 0) &&
-                          (VT::SROW == 0 || 32 % (VT::SROW / VT::SCH) == 0);
+    constexpr bool FAST = chunks_split_warp(KT::ROW, KT::CH) && chunks_split_warp(VT::ROW, VT::CH) &&
+                          chunks_split_warp(KT::SROW, KT::SCH) && chunks_split_warp(VT::SROW, VT::SCH);
     if constexpr (FAST) {
       if (slab_pos >= lo && slab_pos + SLAB <= tok_end) {
         const int ba = blk_s[(slab_pos >> lbs) - p0], bb = blk_s[((slab_pos + 8) >> lbs) - p0];

@@ -373,7 +373,8 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
   constexpr int NK = C::NK;
   constexpr int E = HD / 32;
   constexpr int SLAB = 16;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t tma_smem[];   // (its own name: other kernels declare 128-byte alignment)
+  uint8_t* const smem = tma_smem;
   const uint32_t sbase = tm::saddr(smem);
   if (C::LUT && sbase != (uint32_t)kSmemBase) {   // the tables' placement assumes it
     if (threadIdx.x == 0 && a.err) atomicOr(a.err, 4);
@@ -866,7 +867,6 @@ decode_tma_kernel(const DecodeArgs a, const __grid_constant__ TmaMaps maps, cons
         if constexpr (!PK) tc::mma<false>(o[i], h0, h1, h2, h3, b[2], b[3]);
         tc::mma<false>(o[i], w0, w1, w2, w3, b[0], b[1]);
       };
-      const int tk[4] = {vt0, vt1, vt0 + 8, vt1 + 8};
       if constexpr (VS == S_T3) {
         // (dim, dim+1) pairs of one token: the 6-bit field at bit 6i of the
         // token's span, looked up and regrouped into (first, second) pairs.
