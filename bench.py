@@ -60,9 +60,9 @@ WORKLOAD_DESC = {
 # decode launch, from the ncu capture summarised in profiles/ (None when the
 # kernel changed after the capture).
 TRAFFIC = {
-    ("llama8b", "bf16"): 540_791_040,
-    ("llama8b", "fp8"): 269_581_056,
-    ("llama8b", "turbo4"): 153_384_448,
+    ("llama8b", "bf16"): 540_853_248,
+    ("llama8b", "fp8"): 269_774_848,
+    ("llama8b", "turbo4"): 153_500_160,
 }
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # prefill launch (the slowest format of the workload), from the 1-pass ncu
@@ -80,8 +80,8 @@ PF_TRAFFIC = {
 # peak = 4 warp-instructions per cycle per SM (one per sub-partition) x the
 # SMs x the SM clock sampled during the timed region.
 WARP_INSTR = {
-    ("llama8b", "bf16"): 19_621_407,
-    ("llama8b", "fp8"): 24_304_501,
+    ("llama8b", "bf16"): 19_621_441,
+    ("llama8b", "fp8"): 24_021_319,
     ("llama8b", "turbo4"): 47_024_420,
 }
 
