@@ -246,9 +246,11 @@ size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *                that may run at the same time need separate workspaces.
  *   error_flag   optional device int32
  *
- * One kernel launch: persistent CTAs (two per SM) each take an equal share
- * of all (sequence, kv head) rows' 16-token slabs; rows shared by several
- * CTAs are merged by the last of them to finish. */
+ * One kernel launch: persistent CTAs (one or two per SM) each take an equal
+ * share of all (sequence, kv head) rows' 16-token slabs, each sequence
+ * counted with a fixed extra cost for the unit of work it adds; rows shared
+ * by several CTAs are merged by the last of them to finish, or by the CTA
+ * holding the row's first slab when the others have finished before it. */
 kvq_status kvq_paged_decode(
     const void* q, kvq_dtype q_dtype, int64_t q_stride,
     const void* k_cache, const void* v_cache,
